@@ -1,0 +1,396 @@
+/*
+ * CPU oracle for DSA top-k sparse MLA attention over a paged FP8 (E4M3) KV
+ * cache of 512-dim NoPE latent rows, and for the BF16 -> FP8 paged KV writer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the CUDA library computes.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load it; the library never does,
+ * and it shares no code, header or table with the CUDA sources.
+ *
+ * Sources of each definition:
+ *  - FP8 format: OCP 8-bit floating point specification, E4M3 ("FN") variant:
+ *    bias 7, 3 mantissa bits, S.1111.111 is NaN, largest finite 448, no inf.
+ *    The pages require exactly this flavour and reject E4M3FNUZ on CUDA
+ *    (sgl-project/sglang pull 44012, "Modifications").
+ *  - Raw 512-byte row: 512 unscaled E4M3 bytes (pull 44012, "Modifications",
+ *    "Speed Tests and Profiling"; pull 44217 "[DSA] Support flashmla_sparse_q8
+ *    prefill backend on CUDA", "Modifications").
+ *  - Group-scaled 528-byte row: 512 E4M3 values then four FP32 scales, one per
+ *    128-value group ("[DSA] Support group-scaled FP8 NoPE KV reads for CUDA
+ *    TileLang", "Motivation").  Scale = amax(group)/448, values = e4m3(x/s).
+ *  - Sparse attention: per query token and head, softmax over the scaled dot
+ *    products with the latent rows named by the token's top-k list; -1
+ *    entries are masked (pull 44217, "Modifications": padding with -1); the
+ *    output is the softmax-weighted sum of the same rows (MLA with the
+ *    absorbed NoPE latent, kv_lora_rank = 512, RoPE dim 0) plus the log-sum-exp.
+ *
+ * Readings taken where the pages are silent, as they shape code here: LSE is
+ * the natural log; duplicates count once per top-k slot; an all-masked token
+ * gives O = 0, LSE = -inf; an index outside
+ * the pool or the page table is masked and reported through an error bit;
+ * a zero group gets scale 0 and zero bytes; an input that saturates maps to
+ * +-448; a negative input that rounds to zero keeps its sign (0x80).
+ *
+ * Parity unpinned: NaN inputs (the sign and payload of an encoded NaN).
+ *
+ * Arithmetic: float64 throughout, except where the definition itself fixes
+ * FP32 (the writer's scale amax/448 and the division x/s, which the format
+ * stores as FP32; the FP8 query scale of the same form).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_D 512
+#define ORACLE_GROUP 128
+#define ORACLE_GROUPS 4
+
+/* error bits, same meaning as the library's device flag */
+#define ORACLE_ERR_INDEX_RANGE 1
+#define ORACLE_ERR_PAGE_RANGE 2
+
+/* ---------------------------------------------------------------- FP8 codec */
+
+/* OCP E4M3: sign s, exponent e (4 bits, bias 7), mantissa m (3 bits).
+ * e == 0: subnormal m * 2^-9; otherwise (1 + m/8) * 2^(e-7); 0x7F/0xFF NaN. */
+double oracle_e4m3_decode(uint8_t b) {
+  int s = (b >> 7) & 1;
+  int e = (b >> 3) & 0xF;
+  int m = b & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Saturating round-to-nearest-even encode by exhaustive search: the finite
+ * non-negative code c in [0, 126] nearest to |x|; a tie goes to the even code
+ * (the code's last bit is the mantissa's last bit).  |x| >= 448 (inf too)
+ * gives 0x7E.  The sign bit is copied, so -0 and negative underflow give 0x80. */
+uint8_t oracle_e4m3_encode_bruteforce(float x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  if (isnan(x)) return (uint8_t)(sign | 0x7F);
+  double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 126; ++c) {
+    double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* The same definition with the search done by bisection over the increasing
+ * table of the 127 finite non-negative values (for bulk use; pinned to the
+ * exhaustive search over every BF16 input). */
+static double g_pos_values[127];
+static pthread_once_t g_table_once = PTHREAD_ONCE_INIT;
+static void build_table(void) {
+  for (int c = 0; c <= 126; ++c) g_pos_values[c] = oracle_e4m3_decode((uint8_t)c);
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+  pthread_once(&g_table_once, build_table);
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  if (isnan(x)) return (uint8_t)(sign | 0x7F);
+  double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  int lo = 0, hi = 126; /* invariant: value[lo] <= a < value[hi] (a < 448) */
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (g_pos_values[mid] <= a) lo = mid; else hi = mid;
+  }
+  double dl = a - g_pos_values[lo], dh = g_pos_values[hi] - a;
+  int c;
+  if (dl < dh) c = lo;
+  else if (dh < dl) c = hi;
+  else c = (lo & 1) == 0 ? lo : hi;
+  return (uint8_t)(sign | c);
+}
+
+float oracle_bf16_to_float(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static float le_f32(const uint8_t* p) {
+  uint32_t u = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static void put_le_f32(uint8_t* p, float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  p[0] = (uint8_t)(u & 0xFF);
+  p[1] = (uint8_t)((u >> 8) & 0xFF);
+  p[2] = (uint8_t)((u >> 16) & 0xFF);
+  p[3] = (uint8_t)((u >> 24) & 0xFF);
+}
+
+/* ------------------------------------------------------------------ writers */
+
+/* Raw writer: pool[slot][d] = e4m3(float(x[i][d])), rows with slot < 0 skipped.
+ * Returns the number of rows written, or -1 if a slot is >= pool_rows. */
+int64_t oracle_kv_write_raw(const uint16_t* x, int64_t n_rows, const int64_t* slots,
+                            uint8_t* pool, int64_t pool_rows) {
+  int64_t written = 0;
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t s = slots[i];
+    if (s < 0) continue;
+    if (s >= pool_rows) return -1;
+    uint8_t* row = pool + s * 512;
+    for (int d = 0; d < ORACLE_D; ++d)
+      row[d] = oracle_e4m3_encode(oracle_bf16_to_float(x[i * ORACLE_D + d]));
+    ++written;
+  }
+  return written;
+}
+
+/* One group of 128 values: s = amax/448 in FP32; q = e4m3(x/s) with the FP32
+ * quotient; amax == 0 gives s = 0 and zero bytes. */
+static float scaled_group(const float* v, uint8_t* q) {
+  float amax = 0.0f;
+  for (int i = 0; i < ORACLE_GROUP; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  if (amax == 0.0f) {
+    for (int i = 0; i < ORACLE_GROUP; ++i) q[i] = 0;
+    return 0.0f;
+  }
+  float s = amax / 448.0f;
+  for (int i = 0; i < ORACLE_GROUP; ++i) {
+    float r = v[i] / s;
+    q[i] = oracle_e4m3_encode(r);
+  }
+  return s;
+}
+
+/* Group-scaled writer: row = 512 E4M3 bytes, then 4 little-endian FP32 scales
+ * at byte offsets 512 + 4g; group g covers dims [128g, 128g + 128). */
+int64_t oracle_kv_write_scaled(const uint16_t* x, int64_t n_rows, const int64_t* slots,
+                               uint8_t* pool, int64_t pool_rows) {
+  int64_t written = 0;
+  float v[ORACLE_GROUP];
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t s = slots[i];
+    if (s < 0) continue;
+    if (s >= pool_rows) return -1;
+    uint8_t* row = pool + s * 528;
+    for (int g = 0; g < ORACLE_GROUPS; ++g) {
+      for (int j = 0; j < ORACLE_GROUP; ++j)
+        v[j] = oracle_bf16_to_float(x[i * ORACLE_D + g * ORACLE_GROUP + j]);
+      float sc = scaled_group(v, row + g * ORACLE_GROUP);
+      put_le_f32(row + 512 + 4 * g, sc);
+    }
+    ++written;
+  }
+  return written;
+}
+
+/* FP8 query quantiser: per (token, head) vector of d values,
+ * scale = amax/448 (FP32), q8 = e4m3(q/scale); amax == 0 gives scale 0, zeros. */
+void oracle_quantize_q8(const uint16_t* q, int64_t n_vec, int d, uint8_t* q8, float* scale) {
+  float* v = (float*)malloc(sizeof(float) * (size_t)d);
+  for (int64_t i = 0; i < n_vec; ++i) {
+    float amax = 0.0f;
+    for (int j = 0; j < d; ++j) {
+      v[j] = oracle_bf16_to_float(q[i * d + j]);
+      float a = fabsf(v[j]);
+      if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+      for (int j = 0; j < d; ++j) q8[i * d + j] = 0;
+      scale[i] = 0.0f;
+      continue;
+    }
+    float s = amax / 448.0f;
+    for (int j = 0; j < d; ++j) q8[i * d + j] = oracle_e4m3_encode(v[j] / s);
+    scale[i] = s;
+  }
+  free(v);
+}
+
+/* ---------------------------------------------------------------- attention */
+
+typedef struct {
+  int q_kind;            /* 0: BF16 query, 1: E4M3 query + per-(t,h) FP32 scale */
+  const void* q;         /* [T, H, 512] */
+  const float* q_scale;  /* [T, H] when q_kind == 1 */
+  int T, H;
+  const uint8_t* pool;
+  int64_t pool_rows;
+  int layout;            /* 0: raw512, 1: scaled528 */
+  const int32_t* page_table; /* [B, max_pages] or NULL: indices are physical rows */
+  int B, max_pages, page_size;
+  const int32_t* token_seq;  /* [T] or NULL: every token in sequence 0 */
+  const int32_t* topk;       /* [T, K] */
+  int K;
+  double sm_scale;
+  const int32_t* tokens;     /* which tokens to compute */
+  int n_tokens;
+  double* O;                 /* [n_tokens, H, 512] */
+  double* LSE;               /* [n_tokens, H] */
+  int next;                  /* shared work counter */
+  pthread_mutex_t lock;
+  int err;
+} attn_job;
+
+/* Resolve top-k entry -> physical row, or -1 when masked.  *err gets the bit. */
+static int64_t resolve_row(const attn_job* J, int t, int32_t idx, int* err) {
+  if (idx < 0) return -1;                         /* -1 sentinel (any negative) */
+  if (J->page_table == NULL) {
+    if ((int64_t)idx >= J->pool_rows) { *err |= ORACLE_ERR_INDEX_RANGE; return -1; }
+    return idx;
+  }
+  int seq = J->token_seq ? J->token_seq[t] : 0;
+  if (seq < 0 || seq >= J->B) { *err |= ORACLE_ERR_PAGE_RANGE; return -1; }
+  int page = idx / J->page_size;
+  int off = idx % J->page_size;
+  if (page >= J->max_pages) { *err |= ORACLE_ERR_INDEX_RANGE; return -1; }
+  int32_t phys = J->page_table[(int64_t)seq * J->max_pages + page];
+  if (phys < 0) { *err |= ORACLE_ERR_PAGE_RANGE; return -1; }
+  int64_t row = (int64_t)phys * J->page_size + off;
+  if (row >= J->pool_rows) { *err |= ORACLE_ERR_PAGE_RANGE; return -1; }
+  return row;
+}
+
+/* Dequantised latent row in float64. */
+static void dequant_row(const attn_job* J, int64_t row, double* k) {
+  if (J->layout == 0) {
+    const uint8_t* r = J->pool + row * 512;
+    for (int d = 0; d < ORACLE_D; ++d) k[d] = oracle_e4m3_decode(r[d]);
+  } else {
+    const uint8_t* r = J->pool + row * 528;
+    for (int d = 0; d < ORACLE_D; ++d) {
+      double s = (double)le_f32(r + 512 + 4 * (d / ORACLE_GROUP));
+      k[d] = oracle_e4m3_decode(r[d]) * s;
+    }
+  }
+}
+
+static void attend_token(attn_job* J, int li, double* rows, double* q, double* s, int* err) {
+  int t = J->tokens[li];
+  const int32_t* idx = J->topk + (int64_t)t * J->K;
+  int n = 0;
+  for (int j = 0; j < J->K; ++j) {
+    int64_t row = resolve_row(J, t, idx[j], err);
+    if (row < 0) continue;
+    dequant_row(J, row, rows + (int64_t)n * ORACLE_D);
+    ++n;
+  }
+  for (int h = 0; h < J->H; ++h) {
+    double* o = J->O + ((int64_t)li * J->H + h) * ORACLE_D;
+    int64_t qoff = ((int64_t)t * J->H + h) * ORACLE_D;
+    if (J->q_kind == 0) {
+      const uint16_t* qb = (const uint16_t*)J->q + qoff;
+      for (int d = 0; d < ORACLE_D; ++d) q[d] = (double)oracle_bf16_to_float(qb[d]);
+    } else {
+      const uint8_t* q8 = (const uint8_t*)J->q + qoff;
+      double sc = (double)J->q_scale[(int64_t)t * J->H + h];
+      for (int d = 0; d < ORACLE_D; ++d) q[d] = oracle_e4m3_decode(q8[d]) * sc;
+    }
+    if (n == 0) {                                   /* all masked */
+      for (int d = 0; d < ORACLE_D; ++d) o[d] = 0.0;
+      J->LSE[(int64_t)li * J->H + h] = -INFINITY;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+      const double* k = rows + (int64_t)j * ORACLE_D;
+      double dot = 0.0;
+      for (int d = 0; d < ORACLE_D; ++d) dot += q[d] * k[d];
+      s[j] = J->sm_scale * dot;
+      if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j < n; ++j) l += exp(s[j] - m);
+    double lse = m + log(l);
+    for (int d = 0; d < ORACLE_D; ++d) o[d] = 0.0;
+    for (int j = 0; j < n; ++j) {
+      double p = exp(s[j] - lse);
+      const double* k = rows + (int64_t)j * ORACLE_D;
+      for (int d = 0; d < ORACLE_D; ++d) o[d] += p * k[d];
+    }
+    J->LSE[(int64_t)li * J->H + h] = lse;
+  }
+}
+
+static void* attn_worker(void* arg) {
+  attn_job* J = (attn_job*)arg;
+  double* rows = (double*)malloc(sizeof(double) * (size_t)J->K * ORACLE_D);
+  double* q = (double*)malloc(sizeof(double) * ORACLE_D);
+  double* s = (double*)malloc(sizeof(double) * (size_t)J->K);
+  int err = 0;
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    int li = J->next++;
+    pthread_mutex_unlock(&J->lock);
+    if (li >= J->n_tokens) break;
+    attend_token(J, li, rows, q, s, &err);
+  }
+  pthread_mutex_lock(&J->lock);
+  J->err |= err;
+  pthread_mutex_unlock(&J->lock);
+  free(rows);
+  free(q);
+  free(s);
+  return NULL;
+}
+
+/* O[li, h, :] and LSE[li, h] for each token tokens[li] (all tokens when
+ * tokens == NULL).  Returns the OR of the error bits met. */
+int oracle_sparse_attn(int q_kind, const void* q, const float* q_scale, int T, int H,
+                       const uint8_t* pool, int64_t pool_rows, int layout,
+                       const int32_t* page_table, int B, int max_pages, int page_size,
+                       const int32_t* token_seq, const int32_t* topk, int K, double sm_scale,
+                       const int32_t* tokens, int n_tokens, double* O, double* LSE,
+                       int n_threads) {
+  attn_job J;
+  int32_t* all = NULL;
+  memset(&J, 0, sizeof J);
+  if (tokens == NULL) {
+    all = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    for (int t = 0; t < T; ++t) all[t] = t;
+    tokens = all;
+    n_tokens = T;
+  }
+  J.q_kind = q_kind; J.q = q; J.q_scale = q_scale; J.T = T; J.H = H;
+  J.pool = pool; J.pool_rows = pool_rows; J.layout = layout;
+  J.page_table = page_table; J.B = B; J.max_pages = max_pages; J.page_size = page_size;
+  J.token_seq = token_seq; J.topk = topk; J.K = K; J.sm_scale = sm_scale;
+  J.tokens = tokens; J.n_tokens = n_tokens; J.O = O; J.LSE = LSE;
+  pthread_mutex_init(&J.lock, NULL);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t th[256];
+  for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, attn_worker, &J);
+  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  pthread_mutex_destroy(&J.lock);
+  free(all);
+  return J.err;
+}
+
+/* ------------------------------------------------------- array conveniences */
+
+void oracle_e4m3_encode_array(const float* x, int64_t n, uint8_t* out, int bruteforce) {
+  for (int64_t i = 0; i < n; ++i)
+    out[i] = bruteforce ? oracle_e4m3_encode_bruteforce(x[i]) : oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t* b, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(b[i]);
+}
