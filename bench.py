@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse FP8 MLA attention hot path on GB300.
+
+One step = one pass of the hot path over one batch of the chosen workload:
+the fused BF16 -> FP8 KV writer stores the batch's new latent rows, then the
+sparse attention call (index translation, row gather, dequantisation, QK^T,
+softmax, PV, split-K combine) produces O and LSE for every query token.
+The prefill workload also quantises its queries to FP8 on the GPU first.
+
+Default workload: decode_raw512 (64 query tokens, 16 heads, top-k 2048 over
+a 131072-row raw FP8 pool, page size 64).  L2 is flushed (a 2x-L2 buffer is
+written) before every timed step; steps are timed with CUDA events on the
+launching stream.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference   # the CPU oracle timed on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_mla_attention_page_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sparse-attn query-tokens/s and KV-gather HBM GB/s (fraction of GB300 roofline)"
+UNIT = "query-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_simt.cu"]
+ATTN_KERNEL = "sparse_attn_simt_kernel (+ combine_kernel)"
+COMPUTE_DTYPE = "f32"          # CUDA-core FP32 arithmetic on E4M3 rows
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=list(W.WORKLOADS), default="decode_raw512")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=300)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- workloads
+
+def make_workload(name: str) -> dict:
+    if name == "writer_sweep":
+        return W.writer_sweep(H=16)
+    return W.make(name)
+
+
+def step_rows(w: dict) -> tuple[np.ndarray, np.ndarray]:
+    """The batch's new latent rows (one per query token) and their slots: the
+    last T physical rows of the pool (re-written with the same bytes each step)."""
+    rng = W.rng_for(9000 + w["T"])
+    x = W.f32_to_bf16_bits(rng.standard_normal((w["T"], 512), dtype=np.float32))
+    slots = np.arange(w["pool_rows"] - w["T"], w["pool_rows"], dtype=np.int64)
+    return x, slots
+
+
+def algorithmic_bytes(w: dict) -> int:
+    """Bytes the attention call must move: each valid entry's row once, plus the
+    query, q_scale, top-k list, O and LSE."""
+    T, H, K = w["T"], w["H"], w["K"]
+    R = 512 if w["layout"] == "raw512" else 528
+    valid = W.valid_entry_count(w["topk"])
+    q8 = w["name"] == "prefill_q8_raw512"
+    q_bytes = T * H * 512 * (1 if q8 else 2) + (T * H * 4 if q8 else 0)
+    return valid * R + q_bytes + T * K * 4 + T * H * 512 * 2 + T * H * 4
+
+
+def attn_flops(w: dict) -> int:
+    return 4 * w["H"] * 512 * W.valid_entry_count(w["topk"])
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention call from a committed ncu summary, only while the
+    kernel source is the one that was profiled."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(workload)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_call")
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id is not None:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        used = inside or [min(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[1]]
+        sm = [float(s[0]) for s in used if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in used if s[1].replace(".", "").isdigit()]
+        reasons = sorted({name for s in used for name, v in zip(self.REASONS, s[4:8]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples_in_window": len(inside)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank: int, world: int, local_rank: int, dist):
+    import torch
+
+    from sparse_mla_attention_page_gb300 import binding
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = make_workload(args.workload)
+    T, H, K = w["T"], w["H"], w["K"]
+    layout = w["layout"]
+    prefill = w["name"] == "prefill_q8_raw512"
+
+    def to_dev(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dtype) if dtype is not None else t).to(dev)
+
+    def bf16(a):
+        return to_dev(a.view(np.int16), torch.bfloat16)
+
+    write = binding.dsa_kv_write_raw if layout == "raw512" else binding.dsa_kv_write_scaled
+    pool = torch.zeros(w["pool_rows"], 512 if layout == "raw512" else 528, dtype=torch.uint8, device=dev)
+    kv_src = bf16(w["kv_src"])
+    write(kv_src, to_dev(w["kv_slots"]), pool)
+    del kv_src
+    x_new_h, slots_h = step_rows(w)
+    x_new, slots = bf16(x_new_h), to_dev(slots_h)
+    q = bf16(w["q_bf16"])
+    topk = to_dev(w["topk"])
+    pt = None if w["page_table"] is None else to_dev(w["page_table"])
+    o = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws = binding.workspace_for(T, H, K, device=dev)
+    q8 = torch.empty(T, H, 512, dtype=torch.uint8, device=dev) if prefill else None
+    qs = torch.empty(T, H, dtype=torch.float32, device=dev) if prefill else None
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_write():
+        write(x_new, slots, pool)
+        if prefill:
+            binding.dsa_quantize_q8(q, q8, qs)
+
+    def step_attn():
+        if prefill:
+            binding.dsa_sparse_attn_prefill_q8(q8, qs, pool, layout, topk, w["sm_scale"], o, lse, ws,
+                                               page_table=pt, page_size=w["page_size"])
+        else:
+            binding.dsa_sparse_attn_decode(q, pool, layout, topk, w["sm_scale"], o, lse, ws,
+                                           page_table=pt, page_size=w["page_size"])
+
+    launches_per_step = 1 + (1 if prefill else 0) + 1 + (1 if ws is not None else 0)
+
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        step_write()
+        step_attn()
+    torch.cuda.synchronize(dev)
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush_buf.zero_()
+        ev[i][0].record(stream)
+        step_write()
+        ev[i][1].record(stream)
+        step_attn()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    t_wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = float(sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the public API: inputs from pinned host memory, results back
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_q = pin(w["q_bf16"].view(np.int16)).view(torch.bfloat16)
+    h_topk = pin(w["topk"])
+    h_pt = None if w["page_table"] is None else pin(w["page_table"])
+    h_x = pin(x_new_h.view(np.int16)).view(torch.bfloat16)
+    h_slots = pin(slots_h)
+    h_o = torch.empty(T, H, 512, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_topk, h_x, h_slots) + ((h_pt,) if h_pt is not None else ()))
+    d2h = h_o.numel() * 2 + h_lse.numel() * 4
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
+    for i in range(n_e2e + 3):
+        flush_buf.zero_()
+        if i >= 3:
+            e2e_ev[i - 3][0].record(stream)
+        q.copy_(h_q, non_blocking=True)
+        topk.copy_(h_topk, non_blocking=True)
+        if pt is not None:
+            pt.copy_(h_pt, non_blocking=True)
+        x_new.copy_(h_x, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        step_write()
+        step_attn()
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        if i >= 3:
+            e2e_ev[i - 3][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = float(sum(e[0].elapsed_time(e[1]) for e in e2e_ev))
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    attn_mean_s = statistics.mean(attn_ms) / 1e3
+    abytes = algorithmic_bytes(w)
+    achieved = abytes / attn_mean_s / 1e9
+    traffic = recorded_traffic(args.workload)
+    value = world * T * args.steps / (total_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": COMPUTE_DTYPE,
+        "data": "synthetic (seeded generators; no dataset, no weights)",
+        "config": {"workload": args.workload, "T": T, "H": H, "K": K, "layout": layout,
+                   "pool_rows": w["pool_rows"], "page_size": w["page_size"],
+                   "valid_entries": W.valid_entry_count(w["topk"]),
+                   "step": ("quantize_q8 + " if prefill else "") + f"kv_write_{layout[:3]} of {T} new rows + sparse attention",
+                   "l2": f"flushed before every step ({flush_buf.numel() >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": ATTN_KERNEL, "algorithmic_bytes_per_call": abytes,
+                     "attn_us_per_call": round(attn_mean_s * 1e6, 3),
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                     "tensor_tflops": round(attn_flops(w) / attn_mean_s / 1e12, 2)},
+        "e2e": {"value": round(world * T * n_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    return line, w
+
+
+# ------------------------------------------------------------------- oracle
+
+def oracle_pass(w: dict, pool: np.ndarray, tokens, n_threads: int, q8=None, qs=None):
+    import oracle
+    if q8 is not None:
+        oracle.sparse_attn(pool, w["layout"], w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                           page_table=w["page_table"], page_size=w["page_size"],
+                           tokens=tokens, n_threads=n_threads)
+    else:
+        oracle.sparse_attn(pool, w["layout"], w["topk"], w["sm_scale"], q_bf16=w["q_bf16"],
+                           page_table=w["page_table"], page_size=w["page_size"],
+                           tokens=tokens, n_threads=n_threads)
+
+
+def oracle_setup(w: dict):
+    import oracle
+    pool = oracle.fill_pool(w)
+    q8 = qs = None
+    if w["name"] == "prefill_q8_raw512":
+        q8, qs = oracle.quantize_q8(w["q_bf16"])
+    return pool, q8, qs
+
+
+def cpu_baseline(w: dict, seconds: float) -> dict:
+    """The oracle as it stands, on all host cores, over whole passes of the
+    batch (writer of the step's new rows + attention for every token) until
+    ``seconds`` have passed; for the prefill batch a 64-token slice per pass."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    pool, q8, qs = oracle_setup(w)
+    x_new, slots = step_rows(w)
+    T = w["T"]
+    tokens = np.arange(min(T, 64)) if w["name"] == "prefill_q8_raw512" else np.arange(T)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.kv_write(w["layout"], x_new, slots, pool)
+        oracle_pass(w, pool, tokens, cores, q8, qs)
+        done += len(tokens)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done // len(tokens)} passes x {len(tokens)} tokens of {w['name']} "
+                      f"(writer of the step's rows + float64 attention), {dt:.1f} s"}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return None
+    w = make_workload(args.workload)
+    cores = len(os.sched_getaffinity(0))
+    pool, q8, qs = oracle_setup(w)
+    x_new, slots = step_rows(w)
+    import oracle
+    t0 = time.perf_counter()
+    oracle_pass(w, pool, np.arange(min(cores, w["T"])), cores, q8, qs)
+    per_tok = (time.perf_counter() - t0) / min(cores, w["T"])
+    budget = 120.0
+    n_tok = int(max(1, min(w["T"], budget / max(1, args.steps + args.warmup) / per_tok)))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.kv_write(w["layout"], x_new, slots, pool)
+        oracle_pass(w, pool, np.sort(rng.choice(w["T"], n_tok, replace=False)), cores, q8, qs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kv_write(w["layout"], x_new, slots, pool)
+        oracle_pass(w, pool, np.sort(rng.choice(w["T"], n_tok, replace=False)), cores, q8, qs)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    sample = f"{n_tok} of {w['T']} tokens per step ({w['name']}), writer of the step's rows + float64 attention"
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": args.workload, "T": w["T"], "H": w["H"], "K": w["K"], "layout": w["layout"]},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import importlib
+    importlib.import_module("sparse_mla_attention_page_gb300.build").build()
+    out = run_ours(args, rank, world, local_rank, dist)
+    if out is not None:
+        line, w = out
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

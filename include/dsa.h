@@ -1,0 +1,182 @@
+/*
+ * dsa.h - C ABI of a GB300 (sm_103a) library for DeepSeek-Sparse-Attention
+ * style top-k sparse MLA attention over a paged FP8 (E4M3) KV cache of
+ * 512-dim NoPE latent rows, and for the fused BF16 -> FP8 paged KV writer.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] sglang pull request 44012 (CUDA TileLang raw FP8 KV path), sections
+ *        "Motivation", "Modifications", "Speed Tests and Profiling".
+ *   [P2] "[DSA] Support group-scaled FP8 NoPE KV reads for CUDA TileLang",
+ *        sections "Motivation", "Modifications", "Accuracy Tests".
+ *   [P3] "[DSA] Support flashmla_sparse_q8 prefill backend on CUDA",
+ *        section "Modifications" and the review thread.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are device pointers (cudaMalloc'd or equivalent);
+ *    the caller owns all memory.  The library allocates nothing, keeps no
+ *    state between calls, performs no host<->device copy and no
+ *    synchronisation: each call only enqueues kernels on `stream`
+ *    (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *  - Arguments are validated on the host before anything is launched.  On a
+ *    non-zero status nothing was launched and no output was touched.
+ *    DSA_ERR_CUDA means a launch itself failed (cudaGetLastError).
+ *  - Data-dependent faults (a top-k index outside the pool or the page table,
+ *    a bad page-table entry, a bad destination slot) never trap: the entry
+ *    is skipped and a bit is OR-ed into the caller's int32 *err_flag_dev
+ *    (nullable; the library never clears it).
+ *  - The FP8 format is OCP E4M3 "FN" (max 448, S.1111.111 = NaN) only;
+ *    there is no format argument, so E4M3FNUZ cannot be requested [P1
+ *    Modifications].  Saturating round-to-nearest-even everywhere.
+ *  - Calls on different streams that write the same buffers race.
+ *  - Only GPUs of compute capability 10.3 (GB300) are accepted.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+/* Physical KV row layouts [P1 Modifications; P2 Motivation]:
+ *  DSA_KV_RAW512     512 unscaled E4M3 bytes per row.
+ *  DSA_KV_SCALED528  512 E4M3 bytes, then four little-endian FP32 scales at
+ *                    byte offsets 512 + 4g; scale g applies to dims
+ *                    [128g, 128g + 128): value = e4m3(byte) * scale_g. */
+typedef enum { DSA_KV_RAW512 = 0, DSA_KV_SCALED528 = 1 } dsa_kv_layout;
+
+enum {
+  DSA_OK = 0,
+  DSA_ERR_NULL = 1,      /* a required pointer is NULL */
+  DSA_ERR_SHAPE = 2,     /* a size is negative / zero where it must not be / overflows */
+  DSA_ERR_LAYOUT = 3,    /* unknown layout, or a layout this entry point refuses */
+  DSA_ERR_ROW_WIDTH = 4, /* query width or KV row width is not 512 [P1 Modifications] */
+  DSA_ERR_TOPK_PAD = 5,  /* top-k width is not a positive multiple of 128 [P3 Modifications] */
+  DSA_ERR_HEADS = 6,     /* head count not in {8, 16, 32, 64, 128} */
+  DSA_ERR_WORKSPACE = 7, /* workspace missing or smaller than dsa_sparse_attn_workspace_bytes */
+  DSA_ERR_DEVICE = 8,    /* no current CUDA device of compute capability 10.3 */
+  DSA_ERR_CUDA = 9,      /* a kernel launch failed */
+  DSA_ERR_ALIGN = 10     /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+};
+
+/* Bits OR-ed into *err_flag_dev by the kernels. */
+enum {
+  DSA_DEV_ERR_INDEX_RANGE = 1, /* top-k index beyond the pool (no page table) or beyond
+                                  the page table's width; the entry was masked */
+  DSA_DEV_ERR_PAGE_RANGE = 2,  /* negative page-table entry, page beyond the pool, or a
+                                  token's sequence id outside [0, B); entry masked */
+  DSA_DEV_ERR_TIMEOUT = 4,     /* a bounded wait inside a kernel gave up; the outputs of
+                                  that call are not valid */
+  DSA_DEV_ERR_SLOT_RANGE = 8   /* writer slot >= pool_rows; the row was not written */
+};
+
+/* Human-readable name of a status code (static string). */
+const char* dsa_status_string(int status);
+
+/* Bytes of one physical KV row: 512 or 528 ("exported buffer lengths",
+ * [P1 Speed Tests and Profiling]); 0 for an unknown layout. */
+size_t dsa_kv_row_bytes(int layout);
+
+/* ------------------------------------------------------------- KV writers */
+
+/* Fused cast + paged scatter of new latent rows into a raw512 pool
+ * [P1 Motivation, Modifications: the fused cast/paged writer, selected by
+ * raw versus scaled layout, NoPE rows with no RoPE tensor].
+ *   x_bf16_dev  [n_rows, 512] BF16, row-major, 16-byte aligned.
+ *   slots_dev   [n_rows] int64 physical destination rows; slot < 0 skips the
+ *               row (padding); slot >= pool_rows sets DSA_DEV_ERR_SLOT_RANGE.
+ *   pool_dev    [pool_rows, 512] bytes, 16-byte aligned.
+ *   pool[slot][d] = e4m3_satrne((float)x[i][d]).  Duplicate slots within one
+ *   call are a caller error (which row lands is unspecified).
+ * n_rows == 0 is a no-op returning DSA_OK. */
+int dsa_kv_write_raw(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
+                     void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream);
+
+/* Same for the group-scaled 528-byte layout [P2 Motivation: "512 FP8 values
+ * and four FP32 scales per token"]: for each group g of 128 dims,
+ * s_g = amax_g / 448 (FP32, IEEE division), byte = e4m3_satrne(x / s_g)
+ * (FP32 IEEE division); amax_g == 0 stores s_g = 0 and zero bytes.
+ *   pool_dev  [pool_rows, 528] bytes, 16-byte aligned. */
+int dsa_kv_write_scaled(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
+                        void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream);
+
+/* FP8 query quantiser (NoPE query preparation with a zero-dim RoPE part,
+ * [P3 Modifications: zero-dimensional RoPE queries]): per vector of 512 dims
+ * (one token and head), scale = amax / 448 (FP32), q8 = e4m3_satrne(q / scale);
+ * amax == 0 gives scale 0 and zero bytes.
+ *   q_bf16_dev   [n_vec, 512] BF16;  q8_dev [n_vec, 512] bytes;
+ *   q_scale_dev  [n_vec] float.  All 16-byte aligned except q_scale (4). */
+int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* q_scale_dev,
+                    void* stream);
+
+/* ------------------------------------------------------ sparse attention */
+
+/* Workspace bytes the attention entry points need for (T, H, K) on the
+ * current device (split-K partial results).  May be 0.  Pass at least this
+ * many bytes, 256-byte aligned. */
+size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
+
+/* Sparse MLA decode with BF16 queries over a paged FP8 pool, either layout
+ * [P1 Motivation: TileLang decode over raw FP8 KV; P2 Modifications: the
+ * group-scaled reader; P3 Modifications: top-k padded to a multiple of 128
+ * with -1 sentinels].
+ *
+ * For each token t and head h, over the valid entries j of topk[t]:
+ *   row_j  = page_table[token_seq[t]][i / page_size] * page_size + i % page_size,
+ *            i = topk[t][j]  (row_j = i when page_table is NULL);
+ *   k_j    = dequantised 512-dim latent row (the same row is key and value);
+ *   s_j    = sm_scale * <q[t][h], k_j>;
+ *   LSE    = log(sum_j exp(s_j))            (natural log)
+ *   O[t,h] = sum_j exp(s_j - LSE) * k_j     (BF16, round-to-nearest-even)
+ * A negative index is masked.  A token with no valid entry gets O = 0 and
+ * LSE = -inf.  Duplicate indices count once per slot.
+ *
+ *   q_bf16_dev      [T, H, 512] BF16, 16-byte aligned.
+ *   D, kv_row_dim   must both be 512 (else DSA_ERR_ROW_WIDTH).
+ *   pool_dev        [pool_rows, 512 or 528] bytes, 16-byte aligned.
+ *   page_table_dev  [B, max_pages] int32 physical page ids, or NULL.
+ *   token_seq_dev   [T] int32 sequence id per token, or NULL (all sequence 0).
+ *   topk_dev        [T, K] int32, K a positive multiple of 128.
+ *   o_bf16_dev      [T, H, 512] BF16 out, 16-byte aligned.
+ *   lse_dev         [T, H] float out.
+ *   workspace_dev   ws_bytes >= dsa_sparse_attn_workspace_bytes(T, H, K).
+ *   err_flag_dev    nullable int32 error bits.
+ * H must be one of 8, 16, 32, 64, 128.  T == 0 is a no-op. */
+int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D,
+                           const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
+                           const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                           const int32_t* token_seq_dev, const int32_t* topk_dev, int K,
+                           float sm_scale, void* o_bf16_dev, float* lse_dev,
+                           void* workspace_dev, size_t ws_bytes, int32_t* err_flag_dev,
+                           void* stream);
+
+/* Sparse MLA prefill with FP8 queries ("Q8", [P3 Modifications]): the same
+ * definition with q[t][h][d] = e4m3(q8[t][h][d]) * q_scale[t][h].  Only the
+ * raw 512-byte layout is accepted: a group-scaled pool is refused with
+ * DSA_ERR_LAYOUT, as the pages keep Q8 away from packed/scaled FP8 rows
+ * [P3 review thread: the packed-FP8 KPool guard].
+ *   q8_dev       [T, H, 512] E4M3 bytes, 16-byte aligned.
+ *   q_scale_dev  [T, H] float. */
+int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int T, int H, int D,
+                               const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
+                               const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                               const int32_t* token_seq_dev, const int32_t* topk_dev, int K,
+                               float sm_scale, void* o_bf16_dev, float* lse_dev,
+                               void* workspace_dev, size_t ws_bytes, int32_t* err_flag_dev,
+                               void* stream);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

@@ -1,0 +1,202 @@
+// C ABI entry points (include/dsa.h): host-side validation, then launches.
+// Every check runs before anything is enqueued; on a non-zero status nothing
+// was launched.
+#include <climits>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+#include "kernels.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Current device must be compute capability 10.3; returns its SM count.
+int current_device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DSA_ERR_DEVICE;
+  }
+  int major = 0, minor = 0, count = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DSA_ERR_DEVICE;
+  }
+  if (major != 10 || minor != 3) return DSA_ERR_DEVICE;
+  *sms = count;
+  return DSA_OK;
+}
+
+int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+bool heads_ok(int H) { return H == 8 || H == 16 || H == 32 || H == 64 || H == 128; }
+
+int validate_writer(const void* x, int64_t n_rows, const int64_t* slots, const void* pool,
+                    int64_t pool_rows, int64_t row_bytes) {
+  if (n_rows < 0 || pool_rows < 0) return DSA_ERR_SHAPE;
+  if (n_rows == 0) return DSA_OK;
+  if (x == nullptr || slots == nullptr || pool == nullptr) return DSA_ERR_NULL;
+  if (pool_rows > INT64_MAX / row_bytes || n_rows > INT64_MAX / 1024) return DSA_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(pool, 16) || !aligned(slots, 8)) return DSA_ERR_ALIGN;
+  return DSA_OK;
+}
+
+int write_rows(bool scaled, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
+               int64_t pool_rows, int32_t* err, void* stream) {
+  int st = validate_writer(x, n_rows, slots, pool, pool_rows, scaled ? 528 : 512);
+  if (st != DSA_OK || n_rows == 0) return st;
+  int sms = 0;
+  if ((st = current_device_sms(&sms)) != DSA_OK) return st;
+  cudaGetLastError();  // a stale error from earlier work is not this call's
+  dsa::launch_kv_write(scaled, x, n_rows, slots, pool, pool_rows, err, sms,
+                       static_cast<cudaStream_t>(stream));
+  return launch_status();
+}
+
+int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int D, const void* pool,
+                int64_t pool_rows, int layout, int kv_row_dim, const int32_t* page_table, int B,
+                int max_pages, int page_size, const int32_t* token_seq, const int32_t* topk, int K,
+                float sm_scale, void* o, float* lse, void* ws, size_t ws_bytes, int32_t* err,
+                void* stream) {
+  if (T < 0 || pool_rows < 0) return DSA_ERR_SHAPE;
+  if (D != 512 || kv_row_dim != 512) return DSA_ERR_ROW_WIDTH;
+  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528) return DSA_ERR_LAYOUT;
+  if (q8 && layout != DSA_KV_RAW512) return DSA_ERR_LAYOUT;
+  if (K <= 0 || K % 128 != 0) return DSA_ERR_TOPK_PAD;
+  if (!heads_ok(H)) return DSA_ERR_HEADS;
+  if (T == 0) return DSA_OK;
+  if (q == nullptr || pool == nullptr || topk == nullptr || o == nullptr || lse == nullptr ||
+      (q8 && q_scale == nullptr))
+    return DSA_ERR_NULL;
+  if (pool_rows < 1 || pool_rows > INT32_MAX) return DSA_ERR_SHAPE;
+  if (page_table != nullptr) {
+    if (B < 1 || max_pages < 1 || page_size < 1) return DSA_ERR_SHAPE;
+    if ((int64_t)max_pages * page_size > (int64_t)INT32_MAX + 1) return DSA_ERR_SHAPE;
+  }
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(o, 16) || !aligned(topk, 16) ||
+      !aligned(lse, 4) || (q_scale && !aligned(q_scale, 4)))
+    return DSA_ERR_ALIGN;
+  int sms = 0;
+  int st = current_device_sms(&sms);
+  if (st != DSA_OK) return st;
+  const dsa::SplitPlan plan = dsa::plan_splits(T, H, K, sms);
+  if (plan.ws_bytes > 0) {
+    if (ws == nullptr || ws_bytes < plan.ws_bytes) return DSA_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return DSA_ERR_ALIGN;
+  }
+  dsa::AttnArgs a{};
+  a.q = q;
+  a.q_scale = q_scale;
+  a.T = T;
+  a.H = H;
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.pool_rows = pool_rows;
+  a.scaled = layout == DSA_KV_SCALED528;
+  a.page_table = page_table;
+  a.B = B;
+  a.max_pages = max_pages;
+  a.page_size = page_table ? page_size : 1;
+  a.token_seq = page_table ? token_seq : nullptr;
+  a.topk = topk;
+  a.K = K;
+  a.sm_scale = sm_scale;
+  a.o = o;
+  a.lse = lse;
+  a.ws_o = plan.ws_bytes ? static_cast<float*>(ws) : nullptr;
+  a.ws_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.ws_lse_offset) : nullptr;
+  a.n_splits = plan.n_splits;
+  a.chunk = plan.chunk;
+  a.err = err;
+  cudaGetLastError();
+  dsa::launch_sparse_attn(a, q8, static_cast<cudaStream_t>(stream));
+  return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_NULL: return "DSA_ERR_NULL: a required pointer is NULL";
+    case DSA_ERR_SHAPE: return "DSA_ERR_SHAPE: invalid size";
+    case DSA_ERR_LAYOUT: return "DSA_ERR_LAYOUT: unsupported KV layout for this entry point";
+    case DSA_ERR_ROW_WIDTH: return "DSA_ERR_ROW_WIDTH: query and KV row width must be 512";
+    case DSA_ERR_TOPK_PAD: return "DSA_ERR_TOPK_PAD: top-k width must be a positive multiple of 128";
+    case DSA_ERR_HEADS: return "DSA_ERR_HEADS: head count must be 8, 16, 32, 64 or 128";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace missing or too small";
+    case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE: current device is not a compute capability 10.3 GPU";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA: kernel launch failed";
+    case DSA_ERR_ALIGN: return "DSA_ERR_ALIGN: pointer misaligned";
+    default: return "unknown status";
+  }
+}
+
+size_t dsa_kv_row_bytes(int layout) {
+  if (layout == DSA_KV_RAW512) return 512;
+  if (layout == DSA_KV_SCALED528) return 528;
+  return 0;
+}
+
+int dsa_kv_write_raw(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
+                     void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream) {
+  return write_rows(false, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
+}
+
+int dsa_kv_write_scaled(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
+                        void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream) {
+  return write_rows(true, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
+}
+
+int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* q_scale_dev,
+                    void* stream) {
+  if (n_vec < 0) return DSA_ERR_SHAPE;
+  if (n_vec == 0) return DSA_OK;
+  if (q_bf16_dev == nullptr || q8_dev == nullptr || q_scale_dev == nullptr) return DSA_ERR_NULL;
+  if (n_vec > INT64_MAX / 1024) return DSA_ERR_SHAPE;
+  if (!aligned(q_bf16_dev, 16) || !aligned(q8_dev, 16) || !aligned(q_scale_dev, 4)) return DSA_ERR_ALIGN;
+  int sms = 0;
+  int st = current_device_sms(&sms);
+  if (st != DSA_OK) return st;
+  cudaGetLastError();
+  dsa::launch_quantize_q8(q_bf16_dev, n_vec, q8_dev, q_scale_dev, sms, static_cast<cudaStream_t>(stream));
+  return launch_status();
+}
+
+size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K) {
+  int sms = 0;
+  if (current_device_sms(&sms) != DSA_OK) sms = 152;
+  return dsa::plan_splits(T, H, K, sms).ws_bytes;
+}
+
+int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D, const void* pool_dev,
+                           int64_t pool_rows, int layout, int kv_row_dim,
+                           const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                           const int32_t* token_seq_dev, const int32_t* topk_dev, int K,
+                           float sm_scale, void* o_bf16_dev, float* lse_dev, void* workspace_dev,
+                           size_t ws_bytes, int32_t* err_flag_dev, void* stream) {
+  return sparse_attn(false, q_bf16_dev, nullptr, T, H, D, pool_dev, pool_rows, layout, kv_row_dim,
+                     page_table_dev, B, max_pages, page_size, token_seq_dev, topk_dev, K, sm_scale,
+                     o_bf16_dev, lse_dev, workspace_dev, ws_bytes, err_flag_dev, stream);
+}
+
+int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int T, int H, int D,
+                               const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
+                               const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                               const int32_t* token_seq_dev, const int32_t* topk_dev, int K,
+                               float sm_scale, void* o_bf16_dev, float* lse_dev,
+                               void* workspace_dev, size_t ws_bytes, int32_t* err_flag_dev,
+                               void* stream) {
+  return sparse_attn(true, q8_dev, q_scale_dev, T, H, D, pool_dev, pool_rows, layout, kv_row_dim,
+                     page_table_dev, B, max_pages, page_size, token_seq_dev, topk_dev, K, sm_scale,
+                     o_bf16_dev, lse_dev, workspace_dev, ws_bytes, err_flag_dev, stream);
+}
+
+}  // extern "C"
