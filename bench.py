@@ -228,7 +228,10 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
         step_attn()
     torch.cuda.synchronize(dev)
 
-    gpu_id = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = None
+    if all(hasattr(props, f) for f in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+        gpu_id = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
     sampler = ClockSampler(gpu_id)
     sampler.start()
     time.sleep(0.3)

@@ -44,5 +44,11 @@ struct SplitPlan {
 SplitPlan plan_splits(int T, int H, int K, int sms);
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
+void launch_combine(const AttnArgs& a, cudaStream_t stream);
+
+// Heads handled by one CTA of the attention kernel, and the most top-k
+// entries one CTA can own (bounds the split plan).
+int head_group(int H);
+int max_chunk();
 
 }  // namespace dsa

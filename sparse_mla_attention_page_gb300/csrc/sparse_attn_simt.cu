@@ -192,37 +192,6 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_simt_kernel(AttnArgs a) 
   }
 }
 
-// Merge split-K partials: LSE = logsumexp_s LSE_s, O = sum_s exp(LSE_s - LSE) O_s.
-__global__ void __launch_bounds__(128) combine_kernel(AttnArgs a) {
-  const int64_t th = blockIdx.x;
-  const int64_t TH = (int64_t)a.T * a.H;
-  float m = -INFINITY;
-  for (int s = 0; s < a.n_splits; ++s) m = fmaxf(m, a.ws_lse[s * TH + th]);
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse = -INFINITY;
-  if (m != -INFINITY) {
-    float sum = 0.f;
-    for (int s = 0; s < a.n_splits; ++s) sum += expf(a.ws_lse[s * TH + th] - m);
-    lse = m + logf(sum);
-    for (int s = 0; s < a.n_splits; ++s) {
-      const float ls = a.ws_lse[s * TH + th];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - lse);
-      const float4 v = reinterpret_cast<const float4*>(a.ws_o + (s * TH + th) * kD)[threadIdx.x];
-      o.x = fmaf(w, v.x, o.x);
-      o.y = fmaf(w, v.y, o.y);
-      o.z = fmaf(w, v.z, o.z);
-      o.w = fmaf(w, v.w, o.w);
-    }
-  }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-  uint2 packed;
-  packed.x = *reinterpret_cast<uint32_t*>(&lo);
-  packed.y = *reinterpret_cast<uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + th * kD)[threadIdx.x] = packed;
-  if (threadIdx.x == 0) a.lse[th] = lse;
-}
-
 template <int HG, bool kScaled, bool kQ8>
 void launch_one(const AttnArgs& a, cudaStream_t stream) {
   dim3 grid(a.n_splits, a.T, a.H / HG);
@@ -241,27 +210,6 @@ void launch_one(const AttnArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-SplitPlan plan_splits(int T, int H, int K, int sms) {
-  SplitPlan p{1, K, 0, 0};
-  if (T <= 0 || H <= 0 || K <= 0) return p;
-  const int hg = H >= 16 ? H / 16 : 1;
-  const int64_t units = (int64_t)T * hg;
-  int64_t want = (2LL * sms + units - 1) / units;
-  const int max_splits = K / 128;
-  if (want > max_splits) want = max_splits;
-  if (want < 1) want = 1;
-  int chunk = (int)((K + want - 1) / want);
-  chunk = (chunk + 127) / 128 * 128;
-  p.chunk = chunk;
-  p.n_splits = (K + chunk - 1) / chunk;
-  if (p.n_splits > 1) {
-    const size_t o_bytes = (size_t)p.n_splits * T * H * kD * sizeof(float);
-    p.ws_lse_offset = (o_bytes + 255) / 256 * 256;
-    p.ws_bytes = p.ws_lse_offset + (size_t)p.n_splits * T * H * sizeof(float);
-  }
-  return p;
-}
-
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream) {
   if (a.H >= 16) {
     if (q8) launch_one<16, false, true>(a, stream);
@@ -272,7 +220,11 @@ void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream) {
     else if (a.scaled) launch_one<8, true, false>(a, stream);
     else launch_one<8, false, false>(a, stream);
   }
-  if (a.n_splits > 1) combine_kernel<<<(unsigned)((int64_t)a.T * a.H), 128, 0, stream>>>(a);
+  if (a.n_splits > 1) launch_combine(a, stream);
 }
+
+int head_group(int H) { return H >= 16 ? 16 : 8; }
+
+int max_chunk() { return 1 << 30; }
 
 }  // namespace dsa
