@@ -171,6 +171,40 @@ int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int
                                void* workspace_dev, size_t ws_bytes, int32_t* err_flag_dev,
                                void* stream);
 
+/* ------------------------------------------- decode without allocation */
+
+/* Largest split-K workspace dsa_sparse_attn_decode_noalloc can serve (32 MiB). */
+#define DSA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* dsa_sparse_attn_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that have no way to obtain the workspace buffer: an engine that gives all
+ * of HBM to its KV-cache pool up front, a plug-in running inside a host that
+ * owns the CUDA allocator, or code that must stay free of cudaMalloc.
+ *
+ * Arguments and results are those of dsa_sparse_attn_decode without the
+ * workspace pair.  The workspace is a file-scope device array of
+ * DSA_NOALLOC_SCRATCH_BYTES bytes inside this library: every GPU on which the
+ * library is loaded holds that array until the process exits.  The call
+ * itself allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).
+ *  - The first call on a device looks up the array's device address for that
+ *    device (cudaGetSymbolAddress, with that device current); make that first
+ *    call before any stream capture on the device.
+ *  - A (T, H, K) whose workspace (dsa_sparse_attn_workspace_bytes) exceeds
+ *    DSA_NOALLOC_SCRATCH_BYTES is refused with DSA_ERR_WORKSPACE, nothing
+ *    launched.
+ *  - All calls share the one array, which keeps whatever the last call left
+ *    in it (every byte the kernels read is written first in the same call,
+ *    so nothing needs clearing).  Calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race on it: serialise them. */
+int dsa_sparse_attn_decode_noalloc(const void* q_bf16_dev, int T, int H, int D,
+                                   const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
+                                   const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                                   const int32_t* token_seq_dev, const int32_t* topk_dev, int K,
+                                   float sm_scale, void* o_bf16_dev, float* lse_dev,
+                                   int32_t* err_flag_dev, void* stream);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

@@ -33,7 +33,7 @@ _lib = None
 EXPORTS = (
     "dsa_status_string", "dsa_kv_row_bytes", "dsa_kv_write_raw", "dsa_kv_write_scaled",
     "dsa_quantize_q8", "dsa_sparse_attn_workspace_bytes", "dsa_sparse_attn_decode",
-    "dsa_sparse_attn_prefill_q8",
+    "dsa_sparse_attn_prefill_q8", "dsa_sparse_attn_decode_noalloc",
 )
 
 
@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
             L.dsa_sparse_attn_prefill_q8.argtypes = [
                 vp, vp, i32, i32, i32, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i32,
                 c.c_float, vp, vp, vp, c.c_size_t, vp, vp]
+            L.dsa_sparse_attn_decode_noalloc.restype = i32
+            L.dsa_sparse_attn_decode_noalloc.argtypes = [
+                vp, i32, i32, i32, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i32,
+                c.c_float, vp, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -226,3 +230,17 @@ def dsa_sparse_attn_prefill_q8(q8, q_scale, pool, layout, topk, sm_scale, o, lse
         float(sm_scale), _ptr(o), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err_flag),
         _stream(stream))
     _check(st, "dsa_sparse_attn_prefill_q8")
+
+
+def dsa_sparse_attn_decode_noalloc(q_bf16, pool, layout, topk, sm_scale, o, lse, page_table=None,
+                                   page_size=64, token_seq=None, err_flag=None, stream=None) -> None:
+    """Decode using the library's own static workspace (no allocation by anyone);
+    see include/dsa.h for its size limit and the sharing rules."""
+    _need(q_bf16, "q_bf16", torch.bfloat16, 512)
+    T, H, lay, B, max_pages, _ = _attn_common(q_bf16, pool, layout, topk, o, lse,
+                                              page_table, token_seq, None, err_flag)
+    st = lib().dsa_sparse_attn_decode_noalloc(
+        _ptr(q_bf16), T, H, q_bf16.shape[-1], _ptr(pool), pool.shape[0], lay, _kv_row_dim(pool, lay),
+        _ptr(page_table), B, max_pages, page_size, _ptr(token_seq), _ptr(topk), topk.shape[1],
+        float(sm_scale), _ptr(o), _ptr(lse), _ptr(err_flag), _stream(stream))
+    _check(st, "dsa_sparse_attn_decode_noalloc")
