@@ -38,9 +38,10 @@ from sparse_mla_attention_page_gb300 import workloads as W  # noqa: E402
 METRIC = "sparse-attn query-tokens/s and KV-gather HBM GB/s (fraction of GB300 roofline)"
 UNIT = "query-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_simt.cu"]
-ATTN_KERNEL = "sparse_attn_simt_kernel (+ combine_kernel)"
-COMPUTE_DTYPE = "f32"          # CUDA-core FP32 arithmetic on E4M3 rows
+ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_tc.cu",
+                "sparse_mla_attention_page_gb300/csrc/tc_ptx.cuh"]
+ATTN_KERNEL = "sparse_attn_tc_kernel (+ combine_kernel when split)"
+COMPUTE_DTYPE = "e4m3"         # tcgen05 kind::f8f6f4 MMAs (E4M3 operands, FP32 accumulation)
 
 
 def parse_args():
