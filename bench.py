@@ -4,7 +4,7 @@
 One step = one pass of the hot path over one batch of the chosen workload:
 the fused BF16 -> FP8 KV writer stores the batch's new latent rows, then the
 sparse attention call (index translation, row gather, dequantisation, QK^T,
-softmax, PV, split-K combine) produces O and LSE for every query token.
+softmax, PV, split-K merge) produces O and LSE for every query token.
 The prefill workload also quantises its queries to FP8 on the GPU first.
 
 Default workload: decode_raw512 (64 query tokens, 16 heads, top-k 2048 over
@@ -40,7 +40,7 @@ UNIT = "query-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_tc.cu",
                 "sparse_mla_attention_page_gb300/csrc/tc_ptx.cuh"]
-ATTN_KERNEL = "sparse_attn_tc_kernel (+ combine_kernel when split)"
+ATTN_KERNEL = "prep_query_kernel + sparse_attn_tc_kernel (one attention call)"
 COMPUTE_DTYPE = "e4m3"         # tcgen05 kind::f8f6f4 MMAs (E4M3 operands, FP32 accumulation)
 
 
@@ -221,7 +221,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
             binding.dsa_sparse_attn_decode(q, pool, layout, topk, w["sm_scale"], o, lse, ws,
                                            page_table=pt, page_size=w["page_size"])
 
-    launches_per_step = 1 + (1 if prefill else 0) + 1 + (1 if ws is not None else 0)
+    launches_per_step = 1 + (1 if prefill else 0) + 2      # writer, [q8 quantiser], query pre-pass, attention
 
     for _ in range(args.warmup):
         flush_buf.zero_()

@@ -2,6 +2,8 @@
 // Every check runs before anything is enqueued; on a non-zero status nothing
 // was launched.
 #include <climits>
+#include <cstdio>
+#include <cstdlib>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -31,8 +33,13 @@ int current_device_sms(int* sms) {
   return DSA_OK;
 }
 
+// A failed launch returns DSA_ERR_CUDA; with DSA_DEBUG set in the environment
+// the CUDA error string is also printed to stderr.
 int launch_status() {
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return DSA_OK;
+  if (std::getenv("DSA_DEBUG") != nullptr) std::fprintf(stderr, "dsa: launch failed: %s\n", cudaGetErrorString(e));
+  return DSA_ERR_CUDA;
 }
 
 bool heads_ok(int H) { return H == 8 || H == 16 || H == 32 || H == 64 || H == 128; }
@@ -85,7 +92,7 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   int sms = 0;
   int st = current_device_sms(&sms);
   if (st != DSA_OK) return st;
-  const dsa::SplitPlan plan = dsa::plan_splits(T, H, K, sms);
+  const dsa::AttnPlan plan = dsa::plan_attn(T, H, K, sms);
   if (plan.ws_bytes > 0) {
     if (ws == nullptr || ws_bytes < plan.ws_bytes) return DSA_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return DSA_ERR_ALIGN;
@@ -108,10 +115,17 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   a.sm_scale = sm_scale;
   a.o = o;
   a.lse = lse;
-  a.ws_o = plan.ws_bytes ? static_cast<float*>(ws) : nullptr;
-  a.ws_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.ws_lse_offset) : nullptr;
-  a.n_splits = plan.n_splits;
-  a.chunk = plan.chunk;
+  a.hg = plan.hg;
+  a.hgs = plan.hgs;
+  a.tpt = plan.tpt;
+  a.n_tiles = plan.n_tiles;
+  a.grid = plan.grid;
+  char* wsb = static_cast<char*>(ws);
+  a.qop = reinterpret_cast<uint8_t*>(wsb + plan.qop_offset);
+  a.qsig = reinterpret_cast<float*>(wsb + plan.qsig_offset);
+  a.ws_o = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_o_offset) : nullptr;
+  a.ws_lse = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_lse_offset) : nullptr;
+  a.unit_cnt = plan.split ? reinterpret_cast<int32_t*>(wsb + plan.cnt_offset) : nullptr;
   a.err = err;
   cudaGetLastError();
   dsa::launch_sparse_attn(a, q8, static_cast<cudaStream_t>(stream));
@@ -173,7 +187,7 @@ int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* 
 size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K) {
   int sms = 0;
   if (current_device_sms(&sms) != DSA_OK) sms = 152;
-  return dsa::plan_splits(T, H, K, sms).ws_bytes;
+  return dsa::plan_attn(T, H, K, sms).ws_bytes;
 }
 
 int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D, const void* pool_dev,

@@ -12,6 +12,13 @@ void launch_quantize_q8(const void* q, int64_t n_vec, void* q8, float* scale, in
                         cudaStream_t stream);
 
 // Everything one sparse-attention launch needs.
+//
+// Work is cut into units of (token, group of hg heads) and each unit's top-k
+// list into tiles of 128 entries: n_tiles = T * hgs * tpt.  The persistent
+// kernel runs `grid` CTAs; CTA c owns the contiguous global tiles
+// [c * n_tiles / grid, (c + 1) * n_tiles / grid).  A unit whose tiles span more
+// than one CTA leaves one partial result per CTA; the CTA that finishes the
+// unit's last part merges them.
 struct AttnArgs {
   const void* q;          // BF16 [T,H,512] or E4M3 [T,H,512]
   const float* q_scale;   // [T,H] for FP8 queries, else nullptr
@@ -27,28 +34,42 @@ struct AttnArgs {
   float sm_scale;
   void* o;                // BF16 [T,H,512]
   float* lse;             // [T,H]
-  float* ws_o;            // [n_splits,T,H,512] partial O (normalised), when n_splits > 1
-  float* ws_lse;          // [n_splits,T,H]
-  int n_splits, chunk;    // top-k entries [s*chunk, min(K,(s+1)*chunk)) go to split s
+  int hg, hgs, tpt;       // heads per unit, units per token, tiles per unit
+  int64_t n_tiles;
+  int grid;
+  uint8_t* qop;           // [units][query operand bytes]: FP8 operand image, built by the pre-pass
+  float* qsig;            // [units][query operand rows]: log2-domain multiplier per score column
+  float* ws_o;            // [grid][2][hg][512] normalised partial O (slot 0: the CTA's first unit)
+  float* ws_lse;          // [grid][2][hg]
+  int32_t* unit_cnt;      // [units] parts of a split unit finished so far (zeroed by the pre-pass)
   int32_t* err;
 };
 
-// Split-K plan: how many top-k chunks per token, shared by the workspace
-// query and the launch.
-struct SplitPlan {
-  int n_splits;
-  int chunk;
+// Launch plan shared by the workspace query and the launch.  Workspace:
+// query operands (sized for BF16 queries, the larger case), their column
+// multipliers, then split-K partials when a unit spans two CTAs.
+struct AttnPlan {
+  int hg, hgs, tpt;
+  int64_t n_tiles;
+  int grid;
+  bool split;
+  size_t qop_offset, qsig_offset, ws_o_offset, ws_lse_offset, cnt_offset;
   size_t ws_bytes;
-  size_t ws_lse_offset;
 };
-SplitPlan plan_splits(int T, int H, int K, int sms);
+AttnPlan plan_attn(int T, int H, int K, int sms);
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
-void launch_combine(const AttnArgs& a, cudaStream_t stream);
 
-// Heads handled by one CTA of the attention kernel, and the most top-k
-// entries one CTA can own (bounds the split plan).
+// Heads handled together by one CTA of the attention kernel.
 int head_group(int H);
-int max_chunk();
+
+// The persistent schedule: CTA c owns global tiles [tile_begin(c), tile_begin(c + 1)).
+__host__ __device__ __forceinline__ int64_t tile_begin(int c, int64_t n_tiles, int grid) {
+  return (int64_t)c * n_tiles / grid;
+}
+// The CTA that owns global tile x: the largest c with tile_begin(c) <= x.
+__host__ __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t n_tiles, int grid) {
+  return (int)(((x + 1) * grid + n_tiles - 1) / n_tiles - 1);
+}
 
 }  // namespace dsa

@@ -1,0 +1,34 @@
+// Launch plan and workspace layout of the persistent attention kernel.  Units
+// (token, head group) whose tiles span two or more CTAs leave normalised
+// partial results in the workspace; the last CTA to finish a unit merges them.
+#include "dsa_common.cuh"
+#include "kernels.h"
+
+namespace dsa {
+// One persistent CTA per SM (fewer when there are fewer tiles than SMs).
+AttnPlan plan_attn(int T, int H, int K, int sms) {
+  AttnPlan p{};
+  if (T <= 0 || H <= 0 || K <= 0 || sms <= 0) return p;
+  p.hg = head_group(H);
+  p.hgs = H / p.hg;
+  p.tpt = (K + 127) / 128;
+  p.n_tiles = (int64_t)T * p.hgs * p.tpt;
+  p.grid = (int)(p.n_tiles < sms ? p.n_tiles : sms);
+  for (int k = 1; k < p.grid && !p.split; ++k) p.split = tile_begin(k, p.n_tiles, p.grid) % p.tpt != 0;
+  auto align = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t units = (size_t)T * p.hgs;
+  const size_t nq = 2 * (size_t)p.hg;                 // query operand rows (BF16 queries: hi and lo)
+  p.qop_offset = 0;
+  p.qsig_offset = align(units * nq * kD);
+  p.ws_o_offset = align(p.qsig_offset + units * nq * sizeof(float));
+  size_t end = p.ws_o_offset;
+  if (p.split) {
+    p.ws_lse_offset = align(p.ws_o_offset + (size_t)p.grid * 2 * p.hg * kD * sizeof(float));
+    p.cnt_offset = align(p.ws_lse_offset + (size_t)p.grid * 2 * p.hg * sizeof(float));
+    end = p.cnt_offset + units * sizeof(int32_t);
+  }
+  p.ws_bytes = end;
+  return p;
+}
+
+}  // namespace dsa

@@ -1,28 +1,43 @@
 // Sparse MLA attention on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA = (split s, token t, group of HG <= 32 heads).  It owns top-k entries
-// [s*chunk, (s+1)*chunk) of token t:
+// Persistent kernel: one CTA per SM walks a contiguous range of 128-entry tiles
+// of the global work list (unit = token x group of HG <= 32 heads; a unit's
+// top-k list is tpt tiles).  Consecutive tiles of one unit form a segment;
+// each segment ends with an epilogue that writes the unit's O and LSE (or a
+// partial result when the unit spans CTAs).  Warp roles:
 //
-//   prologue   all warps: FP8 query operand in shared memory; the chunk's
-//              indices are translated through the page table and compacted
-//              (masked and out-of-range entries dropped, order kept), so that
-//              tiles of 128 rows are dense except for the last one.
-//   producer   4 warps: gather each tile's 128 latent rows (512 B, plus the
-//              16-byte scale word for 528-byte rows) with 16-byte cp.async
-//              straight into a 128-byte-swizzled K-major tile; a stage is
-//              complete when every producer's copies have landed
-//              (cp.async.mbarrier.arrive.noinc).  Two stages in flight.
-//   MMA        1 thread: S^T = K Q^T   (M = 128 rows, N = query columns, K = 512)
-//              and, one tile behind, O^T += V^T P^T (M = 128 latent dims x 4,
-//              N = 2*HG, K = 128 rows), both kind::f8f6f4 with FP32
-//              accumulators in tensor memory.  The same shared-memory tile is
+//   index      1 warp: translates each tile's 128 top-k entries through the
+//              page table into physical rows (top-k entries fetched three
+//              tiles ahead, page-table reads one tile ahead, so no load
+//              latency sits between tiles), publishes them in a ring of
+//              kRing tiles for the producers together with the tile's
+//              valid-entry bits, and fetches the FP8 query operand of each
+//              new segment with one bulk copy (prepared by
+//              prep_query_kernel, which runs first).
+//   producer   2 warps: gather each tile's rows with 16-byte cp.async into
+//              the 128-byte-swizzled K-major tile, four rows x 128 bytes per
+//              warp instruction (whole 128-byte lines), zero-filling masked
+//              entries (source size 0: no memory read); a stage is complete
+//              when every producer thread's copies have landed
+//              (cp.async.mbarrier.arrive.noinc).  (Row gathers through the
+//              tensor memory accelerator, tile::gather4, move 128 bytes per
+//              request and top out near a quarter of HBM bandwidth per SM.)
+//   MMA        1 thread: S^T = K Q^T (M = 128 rows, N = query columns, K = 512)
+//              and O^T += V^T P^T (M = 128 latent dims x 4, N = P columns,
+//              K = 128 rows), both kind::f8f6f4 with FP32 accumulators in
+//              tensor memory, issued in whatever order their inputs become
+//              ready (one MMA of K=32 occupies the tensor pipe for the same
+//              ~64 cycles for any N up to 128, so the pipe must never wait on
+//              one queue while the other is ready).  The same shared-memory tile is
 //              the K-major A operand of the first and the MN-major A operand
 //              of the second (V = K: one absorbed NoPE latent row).
-//   softmax    4 warps, one thread per tile row (= TMEM lane): combines the
-//              score columns, masks, reduces the tile max per head across the
-//              128 rows, updates a lazy running max (rescaling O in TMEM only
-//              when the max grows by more than 2^8), forms p = 2^(s - m),
-//              accumulates the denominators and writes P as an FP8 operand.
+//   softmax    8 warps, two per TMEM lane quarter, each thread one tile row
+//              (= TMEM lane) and half of the heads: combine the
+//              score columns, mask, reduce the tile max per head across the
+//              128 rows, keep a lazy running max (O in TMEM is rescaled only
+//              when the max grows by more than 2^8), form p = 2^(s - m),
+//              accumulate the denominators, write P as an FP8 operand, and at
+//              the end of a segment normalise O and store it.
 //
 // Exact FP8 operands for BF16 data: a BF16 query q is split per head into
 // hi = e4m3(q * 2^a) and lo = e4m3((q * 2^a - hi) * 16) with a power-of-two
@@ -30,11 +45,13 @@
 // S = K.hi + K.lo/16 loses nothing but FP32 accumulation order.  P is split
 // into three FP8 terms, p ~ hi + mid/16 + lo/256 (about 13 significant bits),
 // because the output is a softmax-weighted sum of rows whose entries can be
-// large while the sum cancels: two terms (8 bits) are not enough there.  For 528-byte rows the four
-// group scales enter S per row (one accumulator per 128-dim group) and P per
-// group (P_g = p * scale_g * 2^-e_g with a per-CTA power of two 2^e_g that
-// bounds the chunk's scales), so the value rows never need dequantising.
+// large while the sum cancels: two terms (8 bits) are not enough there.  For
+// 528-byte rows the four group scales enter S per row (one accumulator per
+// 128-dim group) and P per group (P_g = p * scale_g * 2^-E_g, E_g a running
+// power of two bounding the segment's scales), so value rows are never
+// dequantised in shared memory.
 #include <atomic>
+#include <cstddef>
 #include <cuda_bf16.h>
 
 #include "dsa_common.cuh"
@@ -48,18 +65,53 @@ using namespace tc;
 
 constexpr int kRows = 128;          // top-k entries per tile = MMA M
 constexpr int kStage = 65536;       // one tile: 128 rows x 512 FP8 bytes
-constexpr int kMaxChunk = 2048;     // top-k entries one CTA can own
 constexpr float kTau = 8.0f;        // lazy max threshold (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;
-constexpr int kProdWarps = 4;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
+constexpr int kSmxWarps = 8;        // softmax warps: warp w -> lane quarter w % 4, head half w / 4
+constexpr int kSmxThreads = kSmxWarps * 32;
+constexpr int kMmaWarp = 8;
+constexpr int kIdxWarp = 9;
+constexpr int kProdWarp0 = 10;
+constexpr int kProdWarps = 2;
+constexpr int kThreads = 32 * (kSmxWarps + 2 + kProdWarps);
+constexpr int kRing = 4;            // tiles of translated rows kept ahead of the producers
+constexpr int kScStage = kRows * 16;   // scale words of one tile (528-byte rows)
+constexpr int kSmemLimit = 232448;
+constexpr int kMiscBytes = 6144;
+
+struct Misc {
+  uint64_t kv_full[3];
+  uint64_t kv_empty[3];
+  uint64_t meta_full[3];
+  uint64_t idx_full[kRing];
+  uint64_t idx_free[kRing];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t q_full[2];
+  uint64_t q_free[2];         // released by the softmax warps after a segment's last scores
+  uint64_t p_full[2];
+  uint64_t pv_done[2];        // PV of the tiles that used P buffer b has completed
+  uint64_t mma_final;
+  uint32_t tmem_base;
+  int abort;
+  uint32_t vmask[3][4];       // valid-entry bits of each stage's tile: word k bit l = row 4l + k
+  __align__(16) int32_t ring[kRing][kRows];   // physical row of each entry (-1: masked)
+  float red[2][2][4][16];     // [tile parity][head half][lane quarter][head] tile maxima
+  float red_sc[2][4][4];      // [tile parity][lane quarter][group] maxima of the group scales
+  float red2[2][4][16];       // [head half][lane quarter][head] denominators (epilogue)
+  __align__(16) float qsig[2][64];   // log2-domain multiplier of each score column, per query buffer
+  float linv[32], lse2[32];
+  float mlse[32];
+  int64_t merge_unit[2];
+  int n_merge;
+};
+static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
+static_assert(offsetof(Misc, ring) % 16 == 0 && offsetof(Misc, qsig) % 16 == 0, "vector access alignment");
 
 template <int HG, bool kScaled, bool kQ8>
 struct Cfg {
+  static constexpr int HPT = HG / 2;                           // heads per softmax thread
   static constexpr int G = kScaled ? 4 : 1;                    // score accumulators per tile
   static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : 2 * HG;  // QK^T N (query operand rows)
   static constexpr int NP = (3 * HG + 15) / 16 * 16;          // PV N: P hi, mid, lo rows (+ zero pad)
@@ -72,40 +124,25 @@ struct Cfg {
   static constexpr int USED = O_COL0 + O_COLS;
   static constexpr int TMEM_COLS =
       USED <= 32 ? 32 : USED <= 64 ? 64 : USED <= 128 ? 128 : USED <= 256 ? 256 : 512;
-  static constexpr int NST = 2;                               // KV stages
+  static constexpr int Q_BYTES = NQ * 512;
+  static constexpr int P_BYTES = G * NP * 128;
+  static constexpr int STAGE = kStage + (kScaled ? kScStage : 0);
+  static constexpr int FIXED = kMiscBytes + 1024;             // + alignment slack
+  // shared memory: two P buffers first, then a third KV stage, then a second query buffer
+  static constexpr int NPB = (2 * STAGE + Q_BYTES + 2 * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
+  static constexpr int NST = (3 * STAGE + Q_BYTES + NPB * P_BYTES + FIXED <= kSmemLimit) ? 3 : 2;
+  static constexpr int NQB = (NST * STAGE + 2 * Q_BYTES + NPB * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
   static constexpr int KV_OFF = 0;
   static constexpr int Q_OFF = KV_OFF + NST * kStage;
-  static constexpr int P_OFF = Q_OFF + NQ * 512;
-  static constexpr int SC_OFF = P_OFF + G * NP * 128;
-  static constexpr int ROWS_OFF = SC_OFF + (kScaled ? NST * kRows * 16 : 0);
-  static constexpr int MISC_OFF = ROWS_OFF + kMaxChunk * 4;
+  static constexpr int P_OFF = Q_OFF + NQB * Q_BYTES;
+  static constexpr int SC_OFF = P_OFF + NPB * P_BYTES;
+  static constexpr int MISC_OFF = SC_OFF + (kScaled ? NST * kScStage : 0);
+  static constexpr int SMEM = MISC_OFF + kMiscBytes + 1024;
+  static_assert(HPT >= 4 && HPT <= 16, "heads per softmax thread");
   static_assert(USED <= 512, "tensor memory budget");
+  static_assert(SMEM <= kSmemLimit, "shared memory budget");
   static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && (NP * 128) % 1024 == 0, "operand alignment");
 };
-
-struct Misc {
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t o_done;
-  uint64_t mma_final;
-  uint32_t tmem_base;
-  int abort;
-  int n_valid;
-  float red[2][4][32];
-  float red2[4][32];
-  float qsig[64];
-  float gmax[kThreads / 32][4];
-  float sc_pow[4], sc_inv[4];
-  float linv[32], lse2[32];
-};
-
-template <int HG, bool kScaled, bool kQ8>
-constexpr size_t smem_bytes() {
-  return (size_t)Cfg<HG, kScaled, kQ8>::MISC_OFF + sizeof(Misc) + 1024;
-}
 
 // Byte offset of element (n, k) in a K-major operand of N rows whose K
 // extent is split into 128-byte blocks (block-major), with the 128-byte
@@ -144,23 +181,84 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t v16) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-__device__ __forceinline__ void st_shared_u8(uint8_t* p, uint32_t v) {
-  asm volatile("st.shared.u8 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+__device__ __forceinline__ void st_shared_u8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// ------------------------------------------------------------- prologue
+// 16-byte copy; bytes beyond src_bytes (0 or 16) are zero-filled and not read.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
 
-// Query operand rows: decode -> [hi heads | lo heads] (exact split of BF16),
-// Q8 -> the FP8 bytes (zero rows pad N to 16).  qsig[c] is the log2-domain
-// multiplier of score column c (includes sm_scale and the power-of-two scale).
-template <int HG, bool kScaled, bool kQ8>
-__device__ void prepare_query(const AttnArgs& a, uint8_t* qop, Misc& ms, int t, int h0) {
-  using C = Cfg<HG, kScaled, kQ8>;
+// Smallest power of two >= x (x > 0, finite), as an exponent.
+__device__ __forceinline__ int ceil_log2(float x) {
+  int e;
+  const float f = frexpf(x, &e);     // x = f * 2^e, f in [0.5, 1)
+  return f == 0.5f ? e - 1 : e;
+}
+
+// x * 2^e exactly for |e| up to 252 (two in-range power-of-two factors).
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  const int e1 = e / 2, e2 = e - e1;
+  return __fmul_rn(__fmul_rn(x, __int_as_float((127 + e1) << 23)), __int_as_float((127 + e2) << 23));
+}
+
+// Warp-uniform bounded wait (all lanes agree on the outcome).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Position of a CTA's tiles in the work list, advanced one tile at a time
+// (no 64-bit division per tile): unit = t * hgs + hgi, tile within the unit.
+struct TileCursor {
+  int64_t unit;
+  int tile, t, hgi;
+  __device__ __forceinline__ TileCursor(const AttnArgs& a, int64_t g) {
+    unit = g / a.tpt;
+    tile = (int)(g - unit * a.tpt);
+    t = (int)(unit / a.hgs);
+    hgi = (int)(unit - (int64_t)t * a.hgs);
+  }
+  __device__ __forceinline__ void advance(const AttnArgs& a) {
+    if (++tile == a.tpt) {
+      tile = 0;
+      ++unit;
+      if (++hgi == a.hgs) {
+        hgi = 0;
+        ++t;
+      }
+    }
+  }
+  // first / last tile of a segment (the unit's tiles inside this CTA)
+  __device__ __forceinline__ bool first(int it) const { return it == 0 || tile == 0; }
+  __device__ __forceinline__ bool last(const AttnArgs& a, int it, int n_it) const {
+    return it == n_it - 1 || tile == a.tpt - 1;
+  }
+};
+
+// ------------------------------------------------------------ query operand
+
+// Pre-pass: for every unit (token, head group), the QK^T B operand exactly as
+// it sits in shared memory (K-major, 128-byte swizzle) and the log2-domain
+// multiplier of each score column.  Decode: rows [hi heads | lo heads], the
+// exact two-term FP8 split of the BF16 query with a power-of-two scale per
+// head; Q8: the FP8 bytes (zero rows pad N to 16), multiplier q_scale.
+// One block per unit, one warp per operand row group.
+template <int HG, bool kQ8>
+__global__ void __launch_bounds__(256) prep_query_kernel(const AttnArgs a) {
+  using C = Cfg<HG, false, kQ8>;
+  grid_launch_dependents();          // the attention grid may start its set-up now
+  const int64_t u = blockIdx.x;
+  const int t = (int)(u / a.hgs), h0 = (int)(u - (int64_t)t * a.hgs) * a.hg;
+  if (threadIdx.x == 0 && a.unit_cnt != nullptr) a.unit_cnt[u] = 0;
+  uint8_t* qop = a.qop + u * C::Q_BYTES;
+  float* qsig = a.qsig + u * C::NQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = kThreads / 32;
   const float base_sig = a.sm_scale * kLog2e;
-  if (kQ8) {
-    for (int n = warp; n < C::NQ; n += kWarps) {
+  if constexpr (kQ8) {
+    for (int n = warp; n < C::NQ; n += 8) {
       uint4 v = make_uint4(0, 0, 0, 0);
       float sig = 0.f;
       if (n < HG) {
@@ -169,11 +267,11 @@ __device__ void prepare_query(const AttnArgs& a, uint8_t* qop, Misc& ms, int t, 
         sig = __ldg(a.q_scale + th) * base_sig;
       }
       *reinterpret_cast<uint4*>(qop + kmajor_off<C::NQ>(n, lane * 16)) = v;
-      if (lane == 0) ms.qsig[n] = sig;
+      if (lane == 0) qsig[n] = sig;
     }
     return;
-  }
-  for (int h = warp; h < HG; h += kWarps) {
+  } else {
+  for (int h = warp; h < HG; h += 8) {
     const int64_t th = (int64_t)t * a.H + h0 + h;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * kD + lane * 16);
     const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
@@ -192,64 +290,192 @@ __device__ void prepare_query(const AttnArgs& a, uint8_t* qop, Misc& ms, int t, 
     float sig = 0.f;
     if (amax > 0.f && amax <= 3.0e38f) {
       int e;
-      const float f = frexpf(amax, &e);          // amax = f * 2^e, f in [0.5, 1)
-      const int sh = (f <= 0.875f) ? 9 - e : 8 - e;   // largest sh with amax * 2^sh <= 448
+      const float f = frexpf(amax, &e);                // amax = f * 2^e, f in [0.5, 1)
+      const int sh = (f <= 0.875f) ? 9 - e : 8 - e;    // largest sh with amax * 2^sh <= 448
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float y[4], r[4];
+        float y[4], r[4], yh[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) y[k] = ldexpf(x[4 * i + k], sh);
+        for (int j = 0; j < 4; ++j) y[j] = scale_pow2(x[4 * i + j], sh);
         hi[i] = e4m3x4_satrne(y[0], y[1], y[2], y[3]);
-        float yh[4];
         e4m3x4_to_f32(hi[i], yh);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) r[k] = (y[k] - yh[k]) * 16.f;
+        for (int j = 0; j < 4; ++j) r[j] = (y[j] - yh[j]) * 16.f;
         lo[i] = e4m3x4_satrne(r[0], r[1], r[2], r[3]);
       }
-      sig = ldexpf(base_sig, -sh);
+      sig = scale_pow2(base_sig, -sh);
     }
     *reinterpret_cast<uint4*>(qop + kmajor_off<C::NQ>(h, lane * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     *reinterpret_cast<uint4*>(qop + kmajor_off<C::NQ>(HG + h, lane * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if (lane == 0) {
-      ms.qsig[h] = sig;
-      ms.qsig[HG + h] = sig * 0.0625f;
+      qsig[h] = sig;
+      qsig[HG + h] = sig * 0.0625f;
     }
+  }
   }
 }
 
 // ------------------------------------------------------------------ roles
 
+// Index warp: per tile, the physical rows of the 128 top-k entries (lane l
+// owns entries 4l .. 4l + 3) into the ring and the valid bits into the
+// tile's stage; per segment, the bulk copy of the query operand.
 template <int HG, bool kScaled, bool kQ8>
-__device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int ntiles, int n_valid) {
+__device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0, int n_it) {
   using C = Cfg<HG, kScaled, kQ8>;
+  constexpr int kAhead = 3;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort = &ms.abort;
+  int4 win[kAhead];           // top-k entries of tiles it + 1 .. it + kAhead (after the shift)
+  int wseq[kAhead];
+  TileCursor ahead(a, b0);    // the next tile whose entries are loaded
+  auto load_entries = [&](int it2, int4& dst, int& sq) {
+    if (it2 < n_it) {
+      // K is a multiple of 128 and the top-k rows are 16-byte aligned
+      dst = __ldg(reinterpret_cast<const int4*>(a.topk + (int64_t)ahead.t * a.K + ahead.tile * kRows) + lane);
+      sq = a.token_seq ? __ldg(a.token_seq + ahead.t) : 0;
+      ahead.advance(a);
+    } else {
+      dst = make_int4(-1, -1, -1, -1);
+      sq = 0;
+    }
+  };
+  // Translation in two halves so that the page-table loads of tile it + 1 are
+  // in flight while tile it is handed over: issue() checks an entry and
+  // starts its page-table load, finish() completes the physical row.  The
+  // checks and error bits are those of resolve_row().  off: -1 masked or
+  // rejected, -2 row already final (no page table), else the in-page offset.
+  auto issue = [&](const int4& e4, int sq, int32_t (&v)[4], int32_t (&off)[4]) {
+    const int32_t idx[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int32_t e = idx[k];
+      v[k] = -1;
+      off[k] = -1;
+      if (e < 0) continue;
+      if (a.page_table == nullptr) {
+        if ((int64_t)e >= a.pool_rows) set_err(a.err, DSA_DEV_ERR_INDEX_RANGE);
+        else { v[k] = e; off[k] = -2; }
+        continue;
+      }
+      if (sq < 0 || sq >= a.B) { set_err(a.err, DSA_DEV_ERR_PAGE_RANGE); continue; }
+      const int page = e / a.page_size;
+      if (page >= a.max_pages) { set_err(a.err, DSA_DEV_ERR_INDEX_RANGE); continue; }
+      off[k] = e - page * a.page_size;
+      v[k] = __ldg(a.page_table + (int64_t)sq * a.max_pages + page);
+    }
+  };
+  auto finish = [&](const int32_t (&v)[4], const int32_t (&off)[4], int32_t (&rows)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      rows[k] = -1;
+      if (off[k] == -2) { rows[k] = v[k]; continue; }
+      if (off[k] < 0) continue;
+      if (v[k] < 0) { set_err(a.err, DSA_DEV_ERR_PAGE_RANGE); continue; }
+      const int64_t row = (int64_t)v[k] * a.page_size + off[k];
+      if (row >= a.pool_rows) { set_err(a.err, DSA_DEV_ERR_PAGE_RANGE); continue; }
+      rows[k] = (int32_t)row;
+    }
+  };
+  int4 cur_e;
+  int cur_sq;
+  load_entries(0, cur_e, cur_sq);
+#pragma unroll
+  for (int d = 0; d < kAhead; ++d) load_entries(1 + d, win[d], wseq[d]);
+  int32_t pv[4], poff[4];
+  issue(cur_e, cur_sq, pv, poff);
+  TileCursor cur(a, b0);
+  int seg = -1;
+  for (int it = 0; it < n_it; ++it, cur.advance(a)) {
+    const bool first = cur.first(it);
+    if (first) ++seg;
+    int32_t rows[4];
+    finish(pv, poff, rows);
+    // entries of tile it + 1 + kAhead; page-table reads of tile it + 1
+    const int4 nxt = win[0];
+    const int nxt_sq = wseq[0];
+#pragma unroll
+    for (int d = 0; d + 1 < kAhead; ++d) {
+      win[d] = win[d + 1];
+      wseq[d] = wseq[d + 1];
+    }
+    load_entries(it + 1 + kAhead, win[kAhead - 1], wseq[kAhead - 1]);
+    issue(nxt, nxt_sq, pv, poff);
+
+    const int slot = it % kRing, stage = it % C::NST;
+    if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort)) break;
+    *reinterpret_cast<int4*>(&ms.ring[slot][4 * lane]) = make_int4(rows[0], rows[1], rows[2], rows[3]);
+    mbar_arrive(smem_u32(&ms.idx_full[slot]));
+    // valid bits of the stage: it was released by PV(it - NST), which needed
+    // the softmax to be done with the stage's previous tile
+    if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort)) break;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const unsigned vm = __ballot_sync(0xffffffffu, rows[k] >= 0);
+      if (lane == 0) ms.vmask[stage][k] = vm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ms.meta_full[stage]));
+    if (first) {
+      const int qb = seg % C::NQB;
+      if (seg >= C::NQB && !warp_wait(smem_u32(&ms.q_free[qb]), ((seg / C::NQB) - 1) & 1, abort)) break;
+      if (seg == 0) grid_dependency_wait();     // the pre-pass has finished writing the operands
+      if (lane == 0) {
+        const uint32_t qbar = smem_u32(&ms.q_full[qb]);
+        mbar_arrive_expect_tx(qbar, C::Q_BYTES + C::NQ * 4);
+        bulk_copy_g2s(smem_u32(sm + C::Q_OFF + qb * C::Q_BYTES), a.qop + cur.unit * C::Q_BYTES, C::Q_BYTES, qbar);
+        bulk_copy_g2s(smem_u32(&ms.qsig[qb][0]), a.qsig + cur.unit * C::NQ, C::NQ * 4, qbar);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Producers: copy the rows of each tile into its stage.  Warp pw owns tile
+// rows [64 pw, 64 pw + 64); one warp instruction moves 128-byte piece kb of
+// four rows (lane: row 4g + lane / 8, 16-byte chunk lane % 8).
+template <int HG, bool kScaled, bool kQ8>
+__device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it) {
+  using C = Cfg<HG, kScaled, kQ8>;
+  constexpr int kRowsPerWarp = kRows / kProdWarps;   // 64
+  constexpr int R = kScaled ? kScaledRow : kRawRow;
   const int ptid = threadIdx.x - kProdWarp0 * 32;
   const int pw = ptid >> 5, lane = ptid & 31;
-  const int32_t* rows = reinterpret_cast<const int32_t*>(sm + C::ROWS_OFF);
-  constexpr int R = kScaled ? kScaledRow : kRawRow;
+  const int rq = lane >> 3, ch = lane & 7;
   volatile int* abort = &ms.abort;
   const uint32_t kv0 = smem_u32(sm + C::KV_OFF);
-  for (int i = 0; i < ntiles; ++i) {
-    const int stage = i % C::NST;
-    if (i >= C::NST && !mbar_wait(smem_u32(&ms.kv_empty[stage]), ((i / C::NST) - 1) & 1, abort)) break;
+  for (int it = 0; it < n_it; ++it) {
+    const int stage = it % C::NST, slot = it % kRing;
+    if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort)) break;
+    if (!warp_wait(smem_u32(&ms.idx_full[slot]), (it / kRing) & 1, abort)) break;
+    int32_t rows[kRowsPerWarp / 4];
+#pragma unroll
+    for (int g = 0; g < kRowsPerWarp / 4; ++g) rows[g] = ms.ring[slot][kRowsPerWarp * pw + 4 * g + rq];
+    int32_t sc_rows[kRowsPerWarp / 32];
+    if (kScaled) {
+#pragma unroll
+      for (int k = 0; k < kRowsPerWarp / 32; ++k) sc_rows[k] = ms.ring[slot][kRowsPerWarp * pw + 32 * k + lane];
+    }
+    mbar_arrive(smem_u32(&ms.idx_free[slot]));
     const uint32_t base = kv0 + stage * kStage;
 #pragma unroll
-    for (int rg = 0; rg < 4; ++rg) {
-      const int r = 32 * pw + 8 * rg + (lane & 7);
-      const int e = i * kRows + r;
-      const int32_t row = rows[e < n_valid ? e : 0];
-      const uint8_t* src = a.pool + (int64_t)row * R;
-      const uint32_t dst_row = base + (r >> 3) * 1024 + (r & 7) * 128;
+    for (int g = 0; g < kRowsPerWarp / 4; ++g) {
+      const int r = kRowsPerWarp * pw + 4 * g + rq;
+      const int32_t row = rows[g];
+      const uint8_t* src = a.pool + (int64_t)(row >= 0 ? row : 0) * R + ch * 16;
+      const uint32_t n = row >= 0 ? 16u : 0u;
+      const uint32_t dst = base + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
 #pragma unroll
-      for (int cg = 0; cg < 8; ++cg) {
-        const int c = 4 * cg + (lane >> 3);   // 16-byte chunk 0..31 of the row
-        cp_async_16(dst_row + (c >> 3) * 16384 + ((((c & 7) ^ (r & 7))) << 4), src + c * 16);
-      }
+      for (int kb = 0; kb < 4; ++kb) cp_async_16_zfill(dst + kb * 16384, src + kb * 128, n);
     }
     if (kScaled) {
-      const int e = i * kRows + ptid;
-      const int32_t row = rows[e < n_valid ? e : 0];
-      cp_async_16(smem_u32(sm + C::SC_OFF + stage * kRows * 16 + ptid * 16),
-                  a.pool + (int64_t)row * kScaledRow + kD);
+#pragma unroll
+      for (int k = 0; k < kRowsPerWarp / 32; ++k) {
+        const int r = kRowsPerWarp * pw + 32 * k + lane;
+        cp_async_16_zfill(smem_u32(sm + C::SC_OFF + stage * kScStage + r * 16),
+                          a.pool + (int64_t)(sc_rows[k] >= 0 ? sc_rows[k] : 0) * kScaledRow + kD,
+                          sc_rows[k] >= 0 ? 16u : 0u);
+      }
     }
     cp_async_arrive_noinc(smem_u32(&ms.kv_full[stage]));
   }
@@ -257,7 +483,7 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int ntil
 }
 
 template <int HG, bool kScaled, bool kQ8>
-__device__ void mma_role(uint8_t* sm, Misc& ms, uint32_t tmem, int ntiles) {
+__device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it) {
   using C = Cfg<HG, kScaled, kQ8>;
   if ((threadIdx.x & 31) != 0) return;
   volatile int* abort = &ms.abort;
@@ -266,54 +492,84 @@ __device__ void mma_role(uint8_t* sm, Misc& ms, uint32_t tmem, int ntiles) {
   const uint32_t p0 = smem_u32(sm + C::P_OFF);
   constexpr uint32_t kIdQK = idesc_e4m3(C::NQ, false);
   constexpr uint32_t kIdPV = idesc_e4m3(C::NP, true);
-  for (int i = 0; i <= ntiles; ++i) {
-    if (i < ntiles) {
-      const int stage = i % C::NST;
-      if (!mbar_wait(smem_u32(&ms.kv_full[stage]), (i / C::NST) & 1, abort)) break;
-      fence_proxy_async_smem();   // rows landed through cp.async (generic proxy)
-      const uint32_t a_base = kv0 + stage * kStage;
-      bool stop = false;
-#pragma unroll
-      for (int qc = 0; qc < C::NQC; ++qc) {
-        const int u = i * C::NQC + qc, sb = u % C::NS;
-        if (u >= C::NS && !mbar_wait(smem_u32(&ms.s_free[sb]), ((u / C::NS) - 1) & 1, abort)) {
-          stop = true;
-          break;
-        }
+  // Issue whichever is ready: PV of the oldest tile whose P is written, or
+  // the next QK^T chunk whose tile, query and score buffer are in place.
+  int qk_it = 0, qk_qc = 0, pv_j = 0, seg = -1;
+  bool q_ready = false, kv_ready = false;
+  TileCursor qk_cur(a, b0), pv_cur(a, b0);
+  uint64_t idle_since = globaltimer_ns();
+  while (pv_j < n_it) {
+    bool progressed = false;
+    if (pv_j < qk_it) {                                   // QK^T of tile pv_j fully issued
+      const int pb = pv_j % C::NPB;
+      if (mbar_test(smem_u32(&ms.p_full[pb]), (pv_j / C::NPB) & 1)) {
+        const bool pv_first = pv_cur.first(pv_j);
         tc_fence_after();
+        const uint32_t a_base = kv0 + (pv_j % C::NST) * kStage;
+        const uint32_t b_base = p0 + pb * C::P_BYTES;
+#pragma unroll
+        for (int db = 0; db < 4; ++db) {
+#pragma unroll
+          for (int js = 0; js < 4; ++js) {
+            const uint64_t ad = sdesc_sw128(a_base + db * 16384 + js * 4096, 1024, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + (kScaled ? db * (C::NP * 128) : 0) + js * 32, 16, 1024);
+            mma_e4m3(tmem + C::O_COL0 + db * C::NP, ad, bd, kIdPV, (!pv_first || js > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(smem_u32(&ms.kv_empty[pv_j % C::NST]));
+        mma_commit(smem_u32(&ms.pv_done[pb]));
+        ++pv_j;
+        pv_cur.advance(a);
+        progressed = true;
+      }
+    }
+    if (!progressed && qk_it < n_it) {
+      const bool qk_first = qk_cur.first(qk_it);
+      const int stage = qk_it % C::NST;
+      if (qk_qc == 0 && qk_first && !q_ready) {
+        if (mbar_test(smem_u32(&ms.q_full[(seg + 1) % C::NQB]), ((seg + 1) / C::NQB) & 1)) {
+          q_ready = true;
+          ++seg;
+        }
+      }
+      if (qk_qc == 0 && !kv_ready) kv_ready = mbar_test(smem_u32(&ms.kv_full[stage]), (qk_it / C::NST) & 1);
+      const int u = qk_it * C::NQC + qk_qc, sb = u % C::NS;
+      const bool q_ok = !(qk_qc == 0 && qk_first) || q_ready;
+      if (q_ok && kv_ready && (u < C::NS || mbar_test(smem_u32(&ms.s_free[sb]), ((u / C::NS) - 1) & 1))) {
+        fence_proxy_async_smem();   // rows landed through cp.async (generic proxy)
+        tc_fence_after();
+        const uint32_t a_base = kv0 + stage * kStage;
+        const uint32_t b_base = q0 + (seg % C::NQB) * C::Q_BYTES;
         const uint32_t d_base = tmem + sb * C::S_COLS;
         constexpr int kSteps = kScaled ? 4 * C::GC : 16;   // K = 32 per step
 #pragma unroll
         for (int st = 0; st < kSteps; ++st) {
-          const int ks = qc * kSteps + st;                  // global K step, 0..15
+          const int ks = qk_qc * kSteps + st;               // K step over the 512 dims
           const int kb = ks >> 2, kk = ks & 3;
           const uint64_t ad = sdesc_sw128(a_base + kb * 16384 + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(q0 + kb * (C::NQ * 128) + kk * 32, 16, 1024);
-          const uint32_t d = d_base + (kScaled ? (kb - qc * C::GC) * C::NQ : 0);
+          const uint64_t bd = sdesc_sw128(b_base + kb * (C::NQ * 128) + kk * 32, 16, 1024);
+          const uint32_t d = d_base + (kScaled ? (kb - qk_qc * C::GC) * C::NQ : 0);
           const uint32_t acc = kScaled ? (kk > 0 ? 1u : 0u) : (ks > 0 ? 1u : 0u);
           mma_e4m3(d, ad, bd, kIdQK, acc);
         }
         mma_commit(smem_u32(&ms.s_full[sb]));
-      }
-      if (stop) break;
-    }
-    if (i >= 1) {
-      const int j = i - 1, stage = j % C::NST;
-      if (!mbar_wait(smem_u32(&ms.p_full), j & 1, abort)) break;
-      fence_proxy_async_smem();
-      tc_fence_after();
-      const uint32_t a_base = kv0 + stage * kStage;
-#pragma unroll
-      for (int db = 0; db < 4; ++db) {
-#pragma unroll
-        for (int js = 0; js < 4; ++js) {
-          const uint64_t ad = sdesc_sw128(a_base + db * 16384 + js * 4096, 1024, 1024);
-          const uint64_t bd = sdesc_sw128(p0 + (kScaled ? db * (C::NP * 128) : 0) + js * 32, 16, 1024);
-          mma_e4m3(tmem + C::O_COL0 + db * C::NP, ad, bd, kIdPV, (j > 0 || js > 0) ? 1u : 0u);
+        if (++qk_qc == C::NQC) {
+          qk_qc = 0;
+          ++qk_it;
+          qk_cur.advance(a);
+          q_ready = false;
+          kv_ready = false;
         }
+        progressed = true;
       }
-      mma_commit(smem_u32(&ms.kv_empty[stage]));
-      mma_commit(smem_u32(&ms.o_done));
+    }
+    if (progressed) {
+      idle_since = globaltimer_ns();
+    } else if (*abort) {
+      break;
+    } else if (globaltimer_ns() - idle_since > 1000000000ull) {
+      *abort = 1;
+      break;
     }
   }
   // every MMA of this CTA completes before the tensor memory is released
@@ -322,302 +578,426 @@ __device__ void mma_role(uint8_t* sm, Misc& ms, uint32_t tmem, int ntiles) {
   mbar_wait(smem_u32(&ms.mma_final), 0, &no_abort, 2000000000ull);
 }
 
-template <int HG, bool kScaled, bool kQ8>
-__device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int ntiles, int n_valid,
-                             int t, int h0, int split) {
-  using C = Cfg<HG, kScaled, kQ8>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = threadIdx.x;                            // tile row = TMEM lane
-  const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-  volatile int* abort = &ms.abort;
-  uint8_t* pbuf = sm + C::P_OFF;
-  float m_run[HG], l_part[HG];
-  float m_lane = -INFINITY;                               // running max of head `lane`
+// Loads columns [c, c + HPT) of a 32-lane TMEM slice, HPT in {4, 8, 16}.
+template <int HPT>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[HPT]) {
+  if constexpr (HPT == 4) {
+    tmem_ld4(taddr, v);
+  } else {
 #pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    m_run[h] = -INFINITY;
-    l_part[h] = 0.f;
+    for (int c = 0; c < HPT; c += 8) {
+      uint32_t t8[8];
+      tmem_ld8(taddr + c, t8);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[c + k] = t8[k];
+    }
   }
-  bool ok = true;
-  for (int i = 0; i < ntiles; ++i) {
-    const int stage = i % C::NST;
+}
+
+template <int HPT>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[HPT]) {
+  if constexpr (HPT == 4) {
+    tmem_st4(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < HPT; c += 8) {
+      uint32_t t8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t8[k] = v[c + k];
+      tmem_st8(taddr + c, t8);
+    }
+  }
+}
+
+// A unit split across CTAs: after this CTA's partial (normalised O, LSE) is
+// written, count it.  The CTA that brings the count to the unit's number of
+// parts merges them once its own tiles are done (at most two such units per
+// CTA: the first and the last of its range).  The counters were zeroed by
+// the pre-pass of this launch.
+__device__ void count_part(const AttnArgs& a, Misc& ms, int64_t unit) {
+  const int64_t u0 = unit * a.tpt;
+  const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
+  const int c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
+  __threadfence();
+  named_bar_sync(1, kSmxThreads);
+  if (threadIdx.x == 0) {
+    grid_dependency_wait();
+    if (atomicAdd(a.unit_cnt + unit, 1) == c1 - c0) ms.merge_unit[ms.n_merge++] = unit;
+  }
+}
+
+// LSE = logsumexp_c LSE_c and O = sum_c exp(LSE_c - LSE) O_c over the CTAs c
+// holding part of the unit.  Loads are batched so that the merge costs a few
+// L2 round trips, not one per part and head.
+template <int HG>
+__device__ void merge_unit(const AttnArgs& a, Misc& ms, int64_t unit) {
+  const int64_t u0 = unit * a.tpt;
+  const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
+  const int c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
+  const int t = (int)(unit / a.hgs), h0 = (int)(unit - (int64_t)t * a.hgs) * a.hg;
+  auto slot = [&](int c) {
+    return (int64_t)c * 2 + (tile_begin(c, a.n_tiles, a.grid) >= u0 ? 0 : 1);
+  };
+  const int tid = threadIdx.x;
+  if (tid < HG) {
+    float m = -INFINITY;
+#pragma unroll 4
+    for (int c = c0; c <= c1; ++c) m = fmaxf(m, __ldcg(a.ws_lse + slot(c) * a.hg + tid));
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+      float sum = 0.f;
+#pragma unroll 4
+      for (int c = c0; c <= c1; ++c) sum += expf(__ldcg(a.ws_lse + slot(c) * a.hg + tid) - m);
+      lse = m + logf(sum);
+    }
+    ms.mlse[tid] = lse;
+    a.lse[(int64_t)t * a.H + h0 + tid] = lse;
+  }
+  named_bar_sync(1, kSmxThreads);
+  // thread -> 4 dims (d4) of heads hq, hq + 2, hq + 4, ...
+  constexpr int kPer = HG / 2, kChunk = kPer < 8 ? kPer : 8;
+  const int d4 = tid & (kD / 4 - 1), hq = tid >> 7;
+#pragma unroll 1
+  for (int j0 = 0; j0 < kPer; j0 += kChunk) {
+    float4 o[kChunk];
+    float lse[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      lse[j] = ms.mlse[hq + 2 * (j0 + j)];
+    }
+#pragma unroll 1
+    for (int c = c0; c <= c1; ++c) {
+      const int64_t sb = slot(c) * a.hg;
+      float ls[kChunk];
+      float4 v[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const int h = hq + 2 * (j0 + j);
+        ls[j] = __ldcg(a.ws_lse + sb + h);
+        v[j] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (sb + h) * kD) + d4);
+      }
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const float w = ls[j] == -INFINITY ? 0.f : expf(ls[j] - lse[j]);
+        o[j].x = fmaf(w, v[j].x, o[j].x);
+        o[j].y = fmaf(w, v[j].y, o[j].y);
+        o[j].z = fmaf(w, v[j].z, o[j].z);
+        o[j].w = fmaf(w, v[j].w, o[j].w);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int h = hq + 2 * (j0 + j);
+      __nv_bfloat162 lo = __floats2bfloat162_rn(o[j].x, o[j].y), hi = __floats2bfloat162_rn(o[j].z, o[j].w);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + ((int64_t)t * a.H + h0 + h) * kD)[d4] = packed;
+    }
+  }
+  named_bar_sync(1, kSmxThreads);
+}
+
+template <int HG, bool kScaled, bool kQ8>
+__device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it,
+                             int cta) {
+  using C = Cfg<HG, kScaled, kQ8>;
+  constexpr int HPT = C::HPT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, hh = warp >> 2;
+  const int row = 32 * quarter + lane;                    // tile row = TMEM lane
+  const int hbase = hh * HPT;                             // first head of this thread
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+  volatile int* abort = &ms.abort;
+  float m_run[HPT], l_part[HPT];
+  float m_lane = -INFINITY;        // running max of head hbase + (lane % HPT), log2 units
+  int e_grp[4] = {-1000, -1000, -1000, -1000};   // running scale exponents (528-byte rows)
+  int seg = -1;
+  bool ok = true;                  // false once a wait gave up: keep going through every barrier
+  TileCursor cur(a, b0);
+  for (int it = 0; it < n_it; ++it, cur.advance(a)) {
+    const bool first = cur.first(it), last = cur.last(a, it, n_it);
+    const int stage = it % C::NST, pb = it % C::NPB;
+    if (first) {
+      ++seg;
+      const int qb = seg % C::NQB;
+      ok &= mbar_wait(smem_u32(&ms.q_full[qb]), (seg / C::NQB) & 1, abort);
+      m_lane = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < HPT; ++h) {
+        m_run[h] = -INFINITY;
+        l_part[h] = 0.f;
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) e_grp[g] = -1000;
+    }
+    const int qb = seg % C::NQB;
+    ok &= mbar_wait(smem_u32(&ms.meta_full[stage]), (it / C::NST) & 1, abort);
+    const bool valid = (ms.vmask[stage][row & 3] >> (row >> 2)) & 1u;
     float sc4[4] = {1.f, 1.f, 1.f, 1.f};
     if (kScaled) {
-      if (!(ok = mbar_wait(smem_u32(&ms.kv_full[stage]), (i / C::NST) & 1, abort))) break;
-      const float4 v = *reinterpret_cast<const float4*>(sm + C::SC_OFF + stage * kRows * 16 + row * 16);
+      ok &= mbar_wait(smem_u32(&ms.kv_full[stage]), (it / C::NST) & 1, abort);
+      const float4 v = *reinterpret_cast<const float4*>(sm + C::SC_OFF + stage * kScStage + row * 16);
       sc4[0] = v.x; sc4[1] = v.y; sc4[2] = v.z; sc4[3] = v.w;
     }
-    float s2[HG];
+    float s2[HPT];
 #pragma unroll
-    for (int h = 0; h < HG; ++h) s2[h] = 0.f;
+    for (int h = 0; h < HPT; ++h) s2[h] = 0.f;
 #pragma unroll
     for (int qc = 0; qc < C::NQC; ++qc) {
-      const int u = i * C::NQC + qc, sb = u % C::NS;
-      if (!(ok = mbar_wait(smem_u32(&ms.s_full[sb]), (u / C::NS) & 1, abort))) break;
+      const int u = it * C::NQC + qc, sb = u % C::NS;
+      ok &= mbar_wait(smem_u32(&ms.s_full[sb]), (u / C::NS) & 1, abort);
       tc_fence_after();
 #pragma unroll
       for (int gl = 0; gl < C::GC; ++gl) {
         const int g = qc * C::GC + gl;
         const uint32_t cbase = lane_base + sb * C::S_COLS + gl * C::NQ;
+        uint32_t hi[HPT], lo[HPT];
+        tmem_ld_cols<HPT>(cbase + hbase, hi);
+        if (!kQ8) tmem_ld_cols<HPT>(cbase + HG + hbase, lo);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < HG; c0 += 8) {
-          uint32_t hi[8], lo[8];
-          tmem_ld8(cbase + c0, hi);
-          if (!kQ8) tmem_ld8(cbase + HG + c0, lo);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            float v = __uint_as_float(hi[k]) * ms.qsig[c0 + k];
-            if (!kQ8) v = fmaf(__uint_as_float(lo[k]), ms.qsig[HG + c0 + k], v);
-            s2[c0 + k] = kScaled ? fmaf(sc4[g], v, s2[c0 + k]) : v;
-          }
+        for (int k = 0; k < HPT; ++k) {
+          float v = __uint_as_float(hi[k]) * ms.qsig[qb][hbase + k];
+          if (!kQ8) v = fmaf(__uint_as_float(lo[k]), ms.qsig[qb][HG + hbase + k], v);
+          s2[k] = kScaled ? fmaf(sc4[g], v, s2[k]) : v;
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&ms.s_free[sb]));
     }
-    if (!ok) break;
-    if (i * kRows + row >= n_valid) {
+    // the segment's query buffer (operand and column multipliers) is no longer needed
+    if (last) mbar_arrive(smem_u32(&ms.q_free[qb]));
+    if (!valid) {
 #pragma unroll
-      for (int h = 0; h < HG; ++h) s2[h] = -INFINITY;
+      for (int h = 0; h < HPT; ++h) s2[h] = -INFINITY;
     }
-    // tile max per head over the 128 rows
-    float tmp[HG];
+    // tile maxima over the 128 rows: per head, and per scale group
+    float tmp[HPT];
 #pragma unroll
-    for (int h = 0; h < HG; ++h) tmp[h] = s2[h];
-    const float wmax = transpose_reduce<HG, true>(tmp, lane);
-    if (lane < HG) ms.red[i & 1][warp][lane] = wmax;
-    named_bar_sync(1, 128);
-    float tile_max = -INFINITY;
-    if (lane < HG)
-      tile_max = fmaxf(fmaxf(ms.red[i & 1][0][lane], ms.red[i & 1][1][lane]),
-                       fmaxf(ms.red[i & 1][2][lane], ms.red[i & 1][3][lane]));
-    const bool need = lane < HG && tile_max > m_lane + kTau;
+    for (int h = 0; h < HPT; ++h) tmp[h] = s2[h];
+    const float wmax = transpose_reduce<HPT, true>(tmp, lane);
+    if (lane < HPT) ms.red[it & 1][hh][quarter][lane] = wmax;
+    if (kScaled && hh == 0) {
+      float sct[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) sct[g] = valid ? fabsf(sc4[g]) : 0.f;
+      const float wsc = transpose_reduce<4, true>(sct, lane);
+      if (lane < 4) ms.red_sc[it & 1][quarter][lane] = wsc;
+    }
+    named_bar_sync(1, kSmxThreads);
+    const int hl = lane % HPT;
+    const float tile_max = fmaxf(fmaxf(ms.red[it & 1][hh][0][hl], ms.red[it & 1][hh][1][hl]),
+                                 fmaxf(ms.red[it & 1][hh][2][hl], ms.red[it & 1][hh][3][hl]));
+    const bool need = tile_max > m_lane + kTau;
     const unsigned rmask = __ballot_sync(0xffffffffu, need);
     float alpha_lane = 1.f;
     if (need) {
-      alpha_lane = exp2f(m_lane - tile_max);
+      alpha_lane = ex2_approx(m_lane - tile_max);
       m_lane = tile_max;
     }
-    float alpha[HG];
-#pragma unroll
-    for (int h = 0; h < HG; ++h) alpha[h] = 1.f;
     if (rmask) {
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
+      for (int h = 0; h < HPT; ++h) {
         m_run[h] = __shfl_sync(0xffffffffu, m_lane, h);
-        alpha[h] = __shfl_sync(0xffffffffu, alpha_lane, h);
-        l_part[h] *= alpha[h];
+        l_part[h] *= __shfl_sync(0xffffffffu, alpha_lane, h);
       }
     }
-    float p[HG];
+    float beta[4] = {1.f, 1.f, 1.f, 1.f};
+    bool bchange = false;
+    if (kScaled) {
 #pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      p[h] = exp2f(s2[h] - m_run[h]);
-      l_part[h] += p[h];
+      for (int g = 0; g < 4; ++g) {
+        const float mx = fmaxf(fmaxf(ms.red_sc[it & 1][0][g], ms.red_sc[it & 1][1][g]),
+                               fmaxf(ms.red_sc[it & 1][2][g], ms.red_sc[it & 1][3][g]));
+        if (mx > 0.f && mx <= 3.0e38f) {
+          const int e = ceil_log2(mx);
+          if (e > e_grp[g]) {
+            beta[g] = e_grp[g] == -1000 ? 0.f : scale_pow2(1.f, e_grp[g] - e);
+            e_grp[g] = e;
+            bchange = true;
+          }
+        }
+      }
     }
-    // the previous tile's PV has finished: P buffer free, O stable
-    if (i > 0 && !(ok = mbar_wait(smem_u32(&ms.o_done), (i - 1) & 1, abort))) break;
-    tc_fence_after();
-    if (i > 0 && rmask) {
+    // O holds this segment's earlier tiles: rescale it after their PV has finished
+    if (!first && (rmask || bchange)) {
+      float alpha[HPT];
+#pragma unroll
+      for (int h = 0; h < HPT; ++h) alpha[h] = __shfl_sync(0xffffffffu, alpha_lane, h);
+      ok &= mbar_wait(smem_u32(&ms.pv_done[(it - 1) % C::NPB]), ((it - 1) / C::NPB) & 1, abort);
+      tc_fence_after();
 #pragma unroll
       for (int db = 0; db < 4; ++db) {
 #pragma unroll
-        for (int c0 = 0; c0 < C::NP; c0 += 8) {
-          const uint32_t ca = lane_base + C::O_COL0 + db * C::NP + c0;
-          uint32_t v[8];
-          tmem_ld8(ca, v);
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t ca = lane_base + C::O_COL0 + db * C::NP + term * HG + hbase;
+          uint32_t v[HPT];
+          tmem_ld_cols<HPT>(ca, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha[(c0 + k) % HG]);
-          tmem_st8(ca, v);
+          for (int k = 0; k < HPT; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha[k] * beta[db]);
+          tmem_st_cols<HPT>(ca, v);
         }
       }
       tmem_wait_st();
     }
+    // this P buffer was last read by PV(it - NPB)
+    if (it >= C::NPB) ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), ((it / C::NPB) - 1) & 1, abort);
+    const uint32_t pbuf = smem_u32(sm + C::P_OFF + pb * C::P_BYTES);
+    // p = 2^(s - m) (0 while the head has seen no valid entry), denominators, P operand
+#pragma unroll
+    for (int h = 0; h < HPT; ++h) {
+      s2[h] = m_run[h] == -INFINITY ? 0.f : ex2_approx(s2[h] - m_run[h]);
+      l_part[h] += s2[h];
+    }
 #pragma unroll
     for (int g = 0; g < C::G; ++g) {
-      const float mul = kScaled ? sc4[g] * ms.sc_inv[g] : 1.f;
-      uint8_t* pg = pbuf + g * (C::NP * 128);
+      const float mul = kScaled ? (e_grp[g] == -1000 ? 0.f : scale_pow2(sc4[g], -e_grp[g])) : 1.f;
+      const uint32_t pg = pbuf + g * (C::NP * 128);
 #pragma unroll
-      for (int h = 0; h < HG; h += 2) {
-        const float v0 = p[h] * mul, v1 = p[h + 1] * mul;
+      for (int h = 0; h < HPT; h += 2) {
+        const float v0 = s2[h] * mul, v1 = s2[h + 1] * mul;
         const uint32_t hi2 = e4m3x2_satrne(v0, v1);
         const float2 hf = e4m3x2_to_f32x2(hi2);
         const float r0 = (v0 - hf.x) * 16.f, r1 = (v1 - hf.y) * 16.f;
         const uint32_t mid2 = e4m3x2_satrne(r0, r1);
         const float2 mf = e4m3x2_to_f32x2(mid2);
         const uint32_t lo2 = e4m3x2_satrne((r0 - mf.x) * 16.f, (r1 - mf.y) * 16.f);
-        st_shared_u8(pg + kmajor_off<C::NP>(h, row), hi2 & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(h + 1, row), (hi2 >> 8) & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(HG + h, row), mid2 & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(HG + h + 1, row), (mid2 >> 8) & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + h, row), lo2 & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + h + 1, row), (lo2 >> 8) & 0xFFu);
+        const int n = hbase + h;
+        st_shared_u8(pg + kmajor_off<C::NP>(n, row), hi2 & 0xFFu);
+        st_shared_u8(pg + kmajor_off<C::NP>(n + 1, row), (hi2 >> 8) & 0xFFu);
+        st_shared_u8(pg + kmajor_off<C::NP>(HG + n, row), mid2 & 0xFFu);
+        st_shared_u8(pg + kmajor_off<C::NP>(HG + n + 1, row), (mid2 >> 8) & 0xFFu);
+        st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n, row), lo2 & 0xFFu);
+        st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n + 1, row), (lo2 >> 8) & 0xFFu);
       }
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    mbar_arrive(smem_u32(&ms.p_full));
-  }
+    mbar_arrive(smem_u32(&ms.p_full[pb]));
 
-  // ---- epilogue: denominators, O normalisation, stores
-  float tmp[HG];
+    if (!last) continue;
+    // ---- end of a segment: denominators, O normalisation, stores
 #pragma unroll
-  for (int h = 0; h < HG; ++h) tmp[h] = l_part[h];
-  const float wsum = transpose_reduce<HG, false>(tmp, lane);
-  if (lane < HG) ms.red2[warp][lane] = wsum;
-  named_bar_sync(1, 128);
-  if (warp == 0 && lane < HG) {
-    const float l = (ms.red2[0][lane] + ms.red2[1][lane]) + (ms.red2[2][lane] + ms.red2[3][lane]);
-    ms.linv[lane] = l > 0.f ? 1.f / l : 0.f;
-    ms.lse2[lane] = l > 0.f ? m_lane + log2f(l) : -INFINITY;
-  }
-  named_bar_sync(1, 128);
-  const bool have_o = ok && ntiles > 0 &&
-                      mbar_wait(smem_u32(&ms.o_done), (ntiles - 1) & 1, abort);
-  tc_fence_after();
-  const int64_t TH = (int64_t)a.T * a.H;
+    for (int h = 0; h < HPT; ++h) tmp[h] = l_part[h];
+    const float wsum = transpose_reduce<HPT, false>(tmp, lane);
+    if (lane < HPT) ms.red2[hh][quarter][lane] = wsum;
+    named_bar_sync(1, kSmxThreads);
+    if (quarter == 0 && lane < HPT) {
+      const float l = (ms.red2[hh][0][lane] + ms.red2[hh][1][lane]) + (ms.red2[hh][2][lane] + ms.red2[hh][3][lane]);
+      ms.linv[hbase + lane] = l > 0.f ? 1.f / l : 0.f;
+      ms.lse2[hbase + lane] = l > 0.f ? m_lane + log2f(l) : -INFINITY;
+    }
+    named_bar_sync(1, kSmxThreads);
+    ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), (it / C::NPB) & 1, abort);
+    tc_fence_after();
+    const int64_t u0 = cur.unit * a.tpt;
+    const int h0 = cur.hgi * a.hg;
+    const bool whole = cta_of_tile(u0, a.n_tiles, a.grid) == cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
+    const int64_t slot = (int64_t)cta * 2 + (b0 >= u0 ? 0 : 1);
+    constexpr int kCh = HPT < 8 ? HPT : 8;               // columns per TMEM load
 #pragma unroll
-  for (int db = 0; db < 4; ++db) {
-    const int d = db * kRows + row;
-    const float pw = kScaled ? ms.sc_pow[db] : 1.f;
+    for (int db = 0; db < 4; ++db) {
+      const int d = db * kRows + row;
+      const float pw2 = kScaled && e_grp[db] != -1000 ? scale_pow2(1.f, e_grp[db]) : 1.f;
 #pragma unroll
-    for (int c0 = 0; c0 < HG; c0 += 8) {
-      float o[8];
-      if (have_o) {
-        uint32_t hi[8], mid[8], lo[8];
-        const uint32_t ob = lane_base + C::O_COL0 + db * C::NP + c0;
-        tmem_ld8(ob, hi);
-        tmem_ld8(ob + HG, mid);
-        tmem_ld8(ob + 2 * HG, lo);
+      for (int c0 = 0; c0 < HPT; c0 += kCh) {
+        uint32_t hi[kCh], mid[kCh], lo[kCh];
+        const uint32_t ob = lane_base + C::O_COL0 + db * C::NP + hbase + c0;
+        tmem_ld_cols<kCh>(ob, hi);
+        tmem_ld_cols<kCh>(ob + HG, mid);
+        tmem_ld_cols<kCh>(ob + 2 * HG, lo);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kCh; ++k) {
+          const int h = hbase + c0 + k;
+          const float li = ms.linv[h];
           const float acc = fmaf(__uint_as_float(lo[k]), 0.00390625f,
                                  fmaf(__uint_as_float(mid[k]), 0.0625f, __uint_as_float(hi[k])));
-          o[k] = acc * pw * ms.linv[c0 + k];
+          const float o = li == 0.f ? 0.f : acc * pw2 * li;
+          if (whole)
+            static_cast<__nv_bfloat16*>(a.o)[((int64_t)cur.t * a.H + h0 + h) * kD + d] = __float2bfloat16_rn(o);
+          else
+            a.ws_o[(slot * a.hg + h) * kD + d] = o;
         }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) o[k] = 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int64_t th = (int64_t)t * a.H + h0 + c0 + k;
-        if (a.n_splits == 1)
-          static_cast<__nv_bfloat16*>(a.o)[th * kD + d] = __float2bfloat16_rn(o[k]);
-        else
-          a.ws_o[((int64_t)split * TH + th) * kD + d] = o[k];
       }
     }
+    if (quarter == 0 && lane < HPT) {
+      const int h = hbase + lane;
+      const float lse = ms.lse2[h] * kLn2;
+      if (whole) a.lse[(int64_t)cur.t * a.H + h0 + h] = lse;
+      else a.ws_lse[slot * a.hg + h] = lse;
+    }
+    if (!whole) count_part(a, ms, cur.unit);
   }
-  if (warp == 0 && lane < HG) {
-    const int64_t th = (int64_t)t * a.H + h0 + lane;
-    const float lse = ms.lse2[lane] * kLn2;
-    if (a.n_splits == 1) a.lse[th] = lse;
-    else a.ws_lse[(int64_t)split * TH + th] = lse;
+  // units whose last part this CTA finished: merge them now that its own tiles are done
+  if (a.unit_cnt != nullptr) {
+    named_bar_sync(1, kSmxThreads);
+    const int n_merge = ms.n_merge;
+    if (n_merge > 0) __threadfence();
+    for (int i = 0; i < n_merge; ++i) merge_unit<HG>(a, ms, ms.merge_unit[i]);
   }
+  (void)ok;
 }
 
+// 12 warps: three share a sub-partition's 16K registers, so at most 168 each.
 template <int HG, bool kScaled, bool kQ8>
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnArgs a) {
+__global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   using C = Cfg<HG, kScaled, kQ8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Misc& ms = *reinterpret_cast<Misc*>(sm + C::MISC_OFF);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, t = blockIdx.y, h0 = blockIdx.z * HG;
-  const int k_begin = split * a.chunk;
-  const int n_chunk = min(a.K, k_begin + a.chunk) - k_begin;
-  int32_t* rows = reinterpret_cast<int32_t*>(sm + C::ROWS_OFF);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int cta = blockIdx.x;
+  const int64_t b0 = tile_begin(cta, a.n_tiles, a.grid);
+  const int n_it = (int)(tile_begin(cta + 1, a.n_tiles, a.grid) - b0);
 
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(smem_u32(&ms.kv_full[s]), kProdWarps * 32);
       mbar_init(smem_u32(&ms.kv_empty[s]), 1);
-      mbar_init(smem_u32(&ms.s_full[s]), 1);
-      mbar_init(smem_u32(&ms.s_free[s]), kSoftmaxWarps * 32);
+      mbar_init(smem_u32(&ms.meta_full[s]), 1);
     }
-    mbar_init(smem_u32(&ms.p_full), kSoftmaxWarps * 32);
-    mbar_init(smem_u32(&ms.o_done), 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_u32(&ms.idx_full[s]), 32);
+      mbar_init(smem_u32(&ms.idx_free[s]), kProdWarps * 32);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ms.s_full[s]), 1);
+      mbar_init(smem_u32(&ms.s_free[s]), kSmxThreads);
+      mbar_init(smem_u32(&ms.q_full[s]), 1);
+      mbar_init(smem_u32(&ms.q_free[s]), kSmxThreads);
+      mbar_init(smem_u32(&ms.p_full[s]), kSmxThreads);
+      mbar_init(smem_u32(&ms.pv_done[s]), 1);
+    }
     mbar_init(smem_u32(&ms.mma_final), 1);
     ms.abort = 0;
+    ms.n_merge = 0;
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&ms.tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
-  prepare_query<HG, kScaled, kQ8>(a, sm + C::Q_OFF, ms, t, h0);
-
-  // translate the chunk's indices to physical rows (-1: masked)
-  const int seq = a.token_seq ? __ldg(a.token_seq + t) : 0;
-  for (int e = tid; e < n_chunk; e += kThreads) {
-    const int32_t idx = __ldg(a.topk + (int64_t)t * a.K + k_begin + e);
-    rows[e] = (int32_t)resolve_row(idx, a.page_table, a.B, a.max_pages, a.page_size, seq, a.pool_rows, a.err);
-  }
-  __syncthreads();
-  // stable in-place compaction of the valid rows
-  if (warp == 0) {
-    int base = 0;
-    for (int e0 = 0; e0 < n_chunk; e0 += 32) {
-      const int e = e0 + lane;
-      const int32_t r = e < n_chunk ? rows[e] : -1;
-      const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
-      if (r >= 0) rows[base + __popc(m & ((1u << lane) - 1u))] = r;
-      base += __popc(m);
-      __syncwarp();
-    }
-    if (lane == 0) ms.n_valid = base;
-  }
-  __syncthreads();
-  const int n_valid = ms.n_valid;
-  if (kScaled) {
-    // a power of two bounding each group's scales over the chunk
-    float gm[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int e = tid; e < n_valid; e += kThreads) {
-      const float4 s = __ldg(reinterpret_cast<const float4*>(a.pool + (int64_t)rows[e] * kScaledRow + kD));
-      gm[0] = fmaxf(gm[0], fabsf(s.x));
-      gm[1] = fmaxf(gm[1], fabsf(s.y));
-      gm[2] = fmaxf(gm[2], fabsf(s.z));
-      gm[3] = fmaxf(gm[3], fabsf(s.w));
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) gm[g] = warp_max(gm[g]);
-    if (lane == 0) {
-#pragma unroll
-      for (int g = 0; g < 4; ++g) ms.gmax[warp][g] = gm[g];
-    }
-    __syncthreads();
-    if (tid < 4) {
-      float mx = 0.f;
-      for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, ms.gmax[w][tid]);
-      int ex = 0;
-      if (mx > 0.f && mx <= 3.0e38f) {
-        const float f = frexpf(mx, &ex);
-        if (f == 0.5f) ex -= 1;                  // 2^ex >= mx, tight
-      }
-      ms.sc_pow[tid] = ldexpf(1.f, ex);
-      ms.sc_inv[tid] = ldexpf(1.f, -ex);
-    }
-  }
-  // P operand starts zeroed: its padding rows (N rounded up to 16) stay zero
-  for (int i = tid; i < C::G * C::NP * 8; i += kThreads)
+  // the P operands start zeroed: their padding rows (N rounded up to 16) stay zero
+  for (int i = tid; i < C::NPB * C::P_BYTES / 16; i += kThreads)
     reinterpret_cast<uint4*>(sm + C::P_OFF)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
-  const int ntiles = (n_valid + kRows - 1) / kRows;
 
-  if (warp < kSoftmaxWarps)
-    softmax_role<HG, kScaled, kQ8>(a, sm, ms, tmem, ntiles, n_valid, t, h0, split);
+  if (warp < kSmxWarps)
+    softmax_role<HG, kScaled, kQ8>(a, sm, ms, tmem, b0, n_it, cta);
   else if (warp == kMmaWarp)
-    mma_role<HG, kScaled, kQ8>(sm, ms, tmem, ntiles);
+    mma_role<HG, kScaled, kQ8>(a, sm, ms, tmem, b0, n_it);
+  else if (warp == kIdxWarp)
+    index_role<HG, kScaled, kQ8>(a, sm, ms, b0, n_it);
   else
-    producer_role<HG, kScaled, kQ8>(a, sm, ms, ntiles, n_valid);
+    producer_role<HG, kScaled, kQ8>(a, sm, ms, n_it);
 
   tc_fence_before();
   __syncthreads();
@@ -630,23 +1010,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnA
 
 template <int HG, bool kScaled, bool kQ8>
 void launch_tc(const AttnArgs& a, cudaStream_t stream) {
-  constexpr size_t smem = smem_bytes<HG, kScaled, kQ8>();
-  static_assert(smem <= 232448, "shared memory budget");
+  using C = Cfg<HG, kScaled, kQ8>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
-    cudaFuncSetAttribute(sparse_attn_tc_kernel<HG, kScaled, kQ8>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaFuncSetAttribute(sparse_attn_tc_kernel<HG, kScaled, kQ8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return;   // the launch below is skipped; the caller sees the attribute error
     configured.fetch_or(bit);
   }
-  dim3 grid(a.n_splits, a.T, a.H / HG);
-  sparse_attn_tc_kernel<HG, kScaled, kQ8><<<grid, kThreads, smem, stream>>>(a);
+  // programmatic dependent launch: set-up, index translation and the first
+  // row gathers overlap the query pre-pass; operand reads wait for it
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<HG, kScaled, kQ8>, a);
 }
 
 template <int HG>
 void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
+  const unsigned units = (unsigned)((int64_t)a.T * a.hgs);
+  if (q8) prep_query_kernel<HG, true><<<units, 256, 0, stream>>>(a);
+  else prep_query_kernel<HG, false><<<units, 256, 0, stream>>>(a);
   if (q8) launch_tc<HG, false, true>(a, stream);
   else if (a.scaled) launch_tc<HG, true, false>(a, stream);
   else launch_tc<HG, false, false>(a, stream);
@@ -657,13 +1051,9 @@ void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
 int head_group(int H) { return H < 32 ? H : 32; }
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream) {
-  const int hg = head_group(a.H);
-  if (hg == 8) launch_hg<8>(a, q8, stream);
-  else if (hg == 16) launch_hg<16>(a, q8, stream);
+  if (a.hg == 8) launch_hg<8>(a, q8, stream);
+  else if (a.hg == 16) launch_hg<16>(a, q8, stream);
   else launch_hg<32>(a, q8, stream);
-  if (a.n_splits > 1) launch_combine(a, stream);
 }
-
-int max_chunk() { return kMaxChunk; }
 
 }  // namespace dsa
