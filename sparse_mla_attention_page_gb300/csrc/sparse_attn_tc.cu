@@ -102,7 +102,6 @@ struct Misc {
   float red2[2][4][16];       // [head half][lane quarter][head] denominators (epilogue)
   __align__(16) float qsig[2][64];   // log2-domain multiplier of each score column, per query buffer
   float linv[32], lse2[32];
-  float mlse[32];
   int64_t merge_unit[2];
   int n_merge;
 };
@@ -627,76 +626,79 @@ __device__ void count_part(const AttnArgs& a, Misc& ms, int64_t unit) {
 }
 
 // LSE = logsumexp_c LSE_c and O = sum_c exp(LSE_c - LSE) O_c over the CTAs c
-// holding part of the unit.  Loads are batched so that the merge costs a few
-// L2 round trips, not one per part and head.
+// holding part of the unit, folded part by part with a running maximum.
+// Each thread owns 4 dims (d4) of heads hq, hq + 2, ...; the loads of a
+// batch of parts and heads are all issued before any is used, so a merge
+// costs about one L2 round trip per batch instead of one per part and head.
 template <int HG>
-__device__ void merge_unit(const AttnArgs& a, Misc& ms, int64_t unit) {
+__device__ void merge_unit(const AttnArgs& a, int64_t unit) {
   const int64_t u0 = unit * a.tpt;
   const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
   const int c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
   const int t = (int)(unit / a.hgs), h0 = (int)(unit - (int64_t)t * a.hgs) * a.hg;
-  auto slot = [&](int c) {
-    return (int64_t)c * 2 + (tile_begin(c, a.n_tiles, a.grid) >= u0 ? 0 : 1);
-  };
   const int tid = threadIdx.x;
-  if (tid < HG) {
-    float m = -INFINITY;
-#pragma unroll 4
-    for (int c = c0; c <= c1; ++c) m = fmaxf(m, __ldcg(a.ws_lse + slot(c) * a.hg + tid));
-    float lse = -INFINITY;
-    if (m != -INFINITY) {
-      float sum = 0.f;
-#pragma unroll 4
-      for (int c = c0; c <= c1; ++c) sum += expf(__ldcg(a.ws_lse + slot(c) * a.hg + tid) - m);
-      lse = m + logf(sum);
-    }
-    ms.mlse[tid] = lse;
-    a.lse[(int64_t)t * a.H + h0 + tid] = lse;
-  }
-  named_bar_sync(1, kSmxThreads);
-  // thread -> 4 dims (d4) of heads hq, hq + 2, hq + 4, ...
-  constexpr int kPer = HG / 2, kChunk = kPer < 8 ? kPer : 8;
   const int d4 = tid & (kD / 4 - 1), hq = tid >> 7;
+  constexpr int kPer = HG / 2;                 // heads per thread
+  constexpr int kChunk = kPer < 8 ? kPer : 8;  // heads per batch
+  constexpr int kParts = 2;                    // parts per batch
 #pragma unroll 1
   for (int j0 = 0; j0 < kPer; j0 += kChunk) {
-    float4 o[kChunk];
-    float lse[kChunk];
+    float m[kChunk], sum[kChunk];
+    float4 acc[kChunk];
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      lse[j] = ms.mlse[hq + 2 * (j0 + j)];
+      m[j] = -INFINITY;
+      sum[j] = 0.f;
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll 1
-    for (int c = c0; c <= c1; ++c) {
-      const int64_t sb = slot(c) * a.hg;
-      float ls[kChunk];
-      float4 v[kChunk];
+    for (int cb = c0; cb <= c1; cb += kParts) {
+      float ls[kParts][kChunk];
+      float4 v[kParts][kChunk];
 #pragma unroll
-      for (int j = 0; j < kChunk; ++j) {
-        const int h = hq + 2 * (j0 + j);
-        ls[j] = __ldcg(a.ws_lse + sb + h);
-        v[j] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (sb + h) * kD) + d4);
+      for (int pp = 0; pp < kParts; ++pp) {
+        const int c = cb + pp;
+        const bool have = c <= c1;
+        const int64_t sb = ((int64_t)c * 2 + (have && tile_begin(c, a.n_tiles, a.grid) < u0 ? 1 : 0)) * a.hg;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          const int h = hq + 2 * (j0 + j);
+          ls[pp][j] = have ? __ldcg(a.ws_lse + sb + h) : -INFINITY;
+          v[pp][j] = have ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + (sb + h) * kD) + d4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
-      for (int j = 0; j < kChunk; ++j) {
-        const float w = ls[j] == -INFINITY ? 0.f : expf(ls[j] - lse[j]);
-        o[j].x = fmaf(w, v[j].x, o[j].x);
-        o[j].y = fmaf(w, v[j].y, o[j].y);
-        o[j].z = fmaf(w, v[j].z, o[j].z);
-        o[j].w = fmaf(w, v[j].w, o[j].w);
+      for (int pp = 0; pp < kParts; ++pp) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          if (ls[pp][j] == -INFINITY) continue;          // a part with no valid entry adds nothing
+          const float mn = fmaxf(m[j], ls[pp][j]);
+          const float r = expf(m[j] - mn);               // 0 while m is -inf
+          const float w = expf(ls[pp][j] - mn);
+          sum[j] = sum[j] * r + w;
+          acc[j].x = fmaf(w, v[pp][j].x, acc[j].x * r);
+          acc[j].y = fmaf(w, v[pp][j].y, acc[j].y * r);
+          acc[j].z = fmaf(w, v[pp][j].z, acc[j].z * r);
+          acc[j].w = fmaf(w, v[pp][j].w, acc[j].w * r);
+          m[j] = mn;
+        }
       }
     }
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
       const int h = hq + 2 * (j0 + j);
-      __nv_bfloat162 lo = __floats2bfloat162_rn(o[j].x, o[j].y), hi = __floats2bfloat162_rn(o[j].z, o[j].w);
+      const float inv = sum[j] > 0.f ? 1.f / sum[j] : 0.f;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
       uint2 packed;
       packed.x = *reinterpret_cast<uint32_t*>(&lo);
       packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + ((int64_t)t * a.H + h0 + h) * kD)[d4] = packed;
+      const int64_t th = (int64_t)t * a.H + h0 + h;
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + th * kD)[d4] = packed;
+      if (d4 == 0) a.lse[th] = sum[j] > 0.f ? m[j] + logf(sum[j]) : -INFINITY;
     }
   }
-  named_bar_sync(1, kSmxThreads);
 }
 
 template <int HG, bool kScaled, bool kQ8>
@@ -937,7 +939,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     named_bar_sync(1, kSmxThreads);
     const int n_merge = ms.n_merge;
     if (n_merge > 0) __threadfence();
-    for (int i = 0; i < n_merge; ++i) merge_unit<HG>(a, ms, ms.merge_unit[i]);
+    for (int i = 0; i < n_merge; ++i) merge_unit<HG>(a, ms.merge_unit[i]);
   }
   (void)ok;
 }
