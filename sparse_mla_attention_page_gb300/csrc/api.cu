@@ -121,8 +121,6 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   a.n_tiles = plan.n_tiles;
   a.grid = plan.grid;
   char* wsb = static_cast<char*>(ws);
-  a.qop = reinterpret_cast<uint8_t*>(wsb + plan.qop_offset);
-  a.qsig = reinterpret_cast<float*>(wsb + plan.qsig_offset);
   a.ws_o = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_o_offset) : nullptr;
   a.ws_lse = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_lse_offset) : nullptr;
   a.unit_cnt = plan.split ? reinterpret_cast<int32_t*>(wsb + plan.cnt_offset) : nullptr;

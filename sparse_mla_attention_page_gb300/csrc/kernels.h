@@ -37,23 +37,22 @@ struct AttnArgs {
   int hg, hgs, tpt;       // heads per unit, units per token, tiles per unit
   int64_t n_tiles;
   int grid;
-  uint8_t* qop;           // [units][query operand bytes]: FP8 operand image, built by the pre-pass
-  float* qsig;            // [units][query operand rows]: log2-domain multiplier per score column
   float* ws_o;            // [grid][2][hg][512] normalised partial O (slot 0: the CTA's first unit)
   float* ws_lse;          // [grid][2][hg]
-  int32_t* unit_cnt;      // [units] parts of a split unit finished so far (zeroed by the pre-pass)
+  int32_t* unit_cnt;      // [units] parts of a split unit finished so far (zero between calls)
   int32_t* err;
 };
 
-// Launch plan shared by the workspace query and the launch.  Workspace:
-// query operands (sized for BF16 queries, the larger case), their column
-// multipliers, then split-K partials when a unit spans two CTAs.
+// Launch plan shared by the workspace query and the launch.  Workspace (only
+// when a unit spans two or more CTAs): split-K partials and one counter per
+// unit; the counters must be zero before a workspace's first use and every
+// call leaves them at zero.
 struct AttnPlan {
   int hg, hgs, tpt;
   int64_t n_tiles;
   int grid;
   bool split;
-  size_t qop_offset, qsig_offset, ws_o_offset, ws_lse_offset, cnt_offset;
+  size_t ws_o_offset, ws_lse_offset, cnt_offset;
   size_t ws_bytes;
 };
 AttnPlan plan_attn(int T, int H, int K, int sms);

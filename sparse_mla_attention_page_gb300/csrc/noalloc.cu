@@ -23,7 +23,8 @@ namespace {
 constexpr size_t kScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
-__device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+// zero-initialised when the library is loaded (the per-unit counters rely on it)
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};

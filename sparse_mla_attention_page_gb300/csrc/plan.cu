@@ -17,12 +17,9 @@ AttnPlan plan_attn(int T, int H, int K, int sms) {
   for (int k = 1; k < p.grid && !p.split; ++k) p.split = tile_begin(k, p.n_tiles, p.grid) % p.tpt != 0;
   auto align = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t units = (size_t)T * p.hgs;
-  const size_t nq = 2 * (size_t)p.hg;                 // query operand rows (BF16 queries: hi and lo)
-  p.qop_offset = 0;
-  p.qsig_offset = align(units * nq * kD);
-  p.ws_o_offset = align(p.qsig_offset + units * nq * sizeof(float));
-  size_t end = p.ws_o_offset;
+  size_t end = 0;
   if (p.split) {
+    p.ws_o_offset = 0;
     p.ws_lse_offset = align(p.ws_o_offset + (size_t)p.grid * 2 * p.hg * kD * sizeof(float));
     p.cnt_offset = align(p.ws_lse_offset + (size_t)p.grid * 2 * p.hg * sizeof(float));
     end = p.cnt_offset + units * sizeof(int32_t);

@@ -88,8 +88,7 @@ struct Misc {
   uint64_t idx_free[kRing];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t q_full[2];
-  uint64_t q_free[2];         // released by the softmax warps after a segment's last scores
+  uint64_t q_full[2];         // a segment's query operand is built (by the softmax warps)
   uint64_t p_full[2];
   uint64_t pv_done[2];        // PV of the tiles that used P buffer b has completed
   uint64_t mma_final;
@@ -239,86 +238,97 @@ struct TileCursor {
 
 // ------------------------------------------------------------ query operand
 
-// Pre-pass: for every unit (token, head group), the QK^T B operand exactly as
-// it sits in shared memory (K-major, 128-byte swizzle) and the log2-domain
-// multiplier of each score column.  Decode: rows [hi heads | lo heads], the
-// exact two-term FP8 split of the BF16 query with a power-of-two scale per
-// head; Q8: the FP8 bytes (zero rows pad N to 16), multiplier q_scale.
-// One block per unit, one warp per operand row group.
+// The QK^T B operand of one unit (token t, heads h0 .. h0 + HG - 1), built by
+// the 256 softmax threads straight into a query buffer: K-major with the
+// 128-byte swizzle, and the log2-domain multiplier of each score column.
+// BF16 queries: rows [hi heads | lo heads], the exact two-term FP8 split
+// hi = e4m3(q 2^sh), lo = e4m3((q 2^sh - hi) 16) with a power of two 2^sh per
+// head.  FP8 queries: the bytes as they are, multiplier q_scale (rows past HG
+// stay zero).  Thread -> head tid / TPH, dims [DPT (tid % TPH), + DPT).
 template <int HG, bool kQ8>
-__global__ void __launch_bounds__(256) prep_query_kernel(const AttnArgs a) {
-  using C = Cfg<HG, false, kQ8>;
-  grid_launch_dependents();          // the attention grid may start its set-up now
-  const int64_t u = blockIdx.x;
-  const int t = (int)(u / a.hgs), h0 = (int)(u - (int64_t)t * a.hgs) * a.hg;
-  if (threadIdx.x == 0 && a.unit_cnt != nullptr) a.unit_cnt[u] = 0;
-  uint8_t* qop = a.qop + u * C::Q_BYTES;
-  float* qsig = a.qsig + u * C::NQ;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float base_sig = a.sm_scale * kLog2e;
-  if constexpr (kQ8) {
-    for (int n = warp; n < C::NQ; n += 8) {
-      uint4 v = make_uint4(0, 0, 0, 0);
+struct QueryBuild {
+  static constexpr int TPH = kSmxThreads / HG;           // threads per head
+  static constexpr int DPT = kD / TPH;                    // dims per thread
+  static constexpr int NV = kQ8 ? DPT / 16 : DPT / 8;     // 16-byte loads per thread
+  uint4 v[NV];
+  float qs;                                               // FP8 queries: q_scale of the head
+
+  __device__ __forceinline__ void load(const AttnArgs& a, int t, int h0) {
+    const int head = threadIdx.x / TPH, part = threadIdx.x % TPH;
+    const int64_t th = (int64_t)t * a.H + h0 + head;
+    const uint4* src = kQ8 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + th * kD + part * DPT)
+                           : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * kD + part * DPT);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
+    qs = kQ8 ? __ldg(a.q_scale + th) : 0.f;
+  }
+
+  // Writes the operand into qbuf (NQ rows) and the multipliers into qsig.
+  template <int NQ>
+  __device__ __forceinline__ void store(const AttnArgs& a, uint8_t* qbuf, float* qsig) const {
+    const int head = threadIdx.x / TPH, part = threadIdx.x % TPH;
+    const float base_sig = a.sm_scale * kLog2e;
+    if constexpr (kQ8) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(head, part * DPT + 16 * i)) = v[i];
+      if (part == 0) qsig[head] = qs * base_sig;
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(w[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(w[j] >> 16))));
+      }
+#pragma unroll
+      for (int off = TPH / 2; off >= 1; off /= 2) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      int sh = 0;
       float sig = 0.f;
-      if (n < HG) {
-        const int64_t th = (int64_t)t * a.H + h0 + n;
-        v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + th * kD) + lane);
-        sig = __ldg(a.q_scale + th) * base_sig;
+      const bool live = amax > 0.f && amax <= 3.0e38f;
+      if (live) {
+        int e;
+        const float f = frexpf(amax, &e);                // amax = f * 2^e, f in [0.5, 1)
+        sh = (f <= 0.875f) ? 9 - e : 8 - e;              // largest sh with amax * 2^sh <= 448
+        sig = scale_pow2(base_sig, -sh);
       }
-      *reinterpret_cast<uint4*>(qop + kmajor_off<C::NQ>(n, lane * 16)) = v;
-      if (lane == 0) qsig[n] = sig;
-    }
-    return;
-  } else {
-  for (int h = warp; h < HG; h += 8) {
-    const int64_t th = (int64_t)t * a.H + h0 + h;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * kD + lane * 16);
-    const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    float x[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    }
-    float amax = 0.f;
+      for (int c = 0; c < NV / 2; ++c) {                  // 16 dims per chunk
+        uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+        if (live) {
+          const uint32_t w[8] = {v[2 * c].x, v[2 * c].y, v[2 * c].z, v[2 * c].w,
+                                 v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = warp_max(amax);
-    uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-    float sig = 0.f;
-    if (amax > 0.f && amax <= 3.0e38f) {
-      int e;
-      const float f = frexpf(amax, &e);                // amax = f * 2^e, f in [0.5, 1)
-      const int sh = (f <= 0.875f) ? 9 - e : 8 - e;    // largest sh with amax * 2^sh <= 448
+          for (int i = 0; i < 4; ++i) {
+            float y[4], r[4], yh[4];
+            y[0] = scale_pow2(bf16_bits_to_f32(w[2 * i] & 0xFFFFu), sh);
+            y[1] = scale_pow2(bf16_bits_to_f32(w[2 * i] >> 16), sh);
+            y[2] = scale_pow2(bf16_bits_to_f32(w[2 * i + 1] & 0xFFFFu), sh);
+            y[3] = scale_pow2(bf16_bits_to_f32(w[2 * i + 1] >> 16), sh);
+            hi[i] = e4m3x4_satrne(y[0], y[1], y[2], y[3]);
+            e4m3x4_to_f32(hi[i], yh);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float y[4], r[4], yh[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) y[j] = scale_pow2(x[4 * i + j], sh);
-        hi[i] = e4m3x4_satrne(y[0], y[1], y[2], y[3]);
-        e4m3x4_to_f32(hi[i], yh);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) r[j] = (y[j] - yh[j]) * 16.f;
-        lo[i] = e4m3x4_satrne(r[0], r[1], r[2], r[3]);
+            for (int j = 0; j < 4; ++j) r[j] = (y[j] - yh[j]) * 16.f;
+            lo[i] = e4m3x4_satrne(r[0], r[1], r[2], r[3]);
+          }
+        }
+        const int k0 = part * DPT + 16 * c;
+        *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(head, k0)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(HG + head, k0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      sig = scale_pow2(base_sig, -sh);
-    }
-    *reinterpret_cast<uint4*>(qop + kmajor_off<C::NQ>(h, lane * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(qop + kmajor_off<C::NQ>(HG + h, lane * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    if (lane == 0) {
-      qsig[h] = sig;
-      qsig[HG + h] = sig * 0.0625f;
+      if (part == 0) {
+        qsig[head] = sig;
+        qsig[HG + head] = sig * 0.0625f;
+      }
     }
   }
-  }
-}
+};
 
 // ------------------------------------------------------------------ roles
 
 // Index warp: per tile, the physical rows of the 128 top-k entries (lane l
 // owns entries 4l .. 4l + 3) into the ring and the valid bits into the
-// tile's stage; per segment, the bulk copy of the query operand.
+// tile's stage.
 template <int HG, bool kScaled, bool kQ8>
 __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0, int n_it) {
   using C = Cfg<HG, kScaled, kQ8>;
@@ -383,11 +393,7 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
   for (int d = 0; d < kAhead; ++d) load_entries(1 + d, win[d], wseq[d]);
   int32_t pv[4], poff[4];
   issue(cur_e, cur_sq, pv, poff);
-  TileCursor cur(a, b0);
-  int seg = -1;
-  for (int it = 0; it < n_it; ++it, cur.advance(a)) {
-    const bool first = cur.first(it);
-    if (first) ++seg;
+  for (int it = 0; it < n_it; ++it) {
     int32_t rows[4];
     finish(pv, poff, rows);
     // entries of tile it + 1 + kAhead; page-table reads of tile it + 1
@@ -415,18 +421,6 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&ms.meta_full[stage]));
-    if (first) {
-      const int qb = seg % C::NQB;
-      if (seg >= C::NQB && !warp_wait(smem_u32(&ms.q_free[qb]), ((seg / C::NQB) - 1) & 1, abort)) break;
-      if (seg == 0) grid_dependency_wait();     // the pre-pass has finished writing the operands
-      if (lane == 0) {
-        const uint32_t qbar = smem_u32(&ms.q_full[qb]);
-        mbar_arrive_expect_tx(qbar, C::Q_BYTES + C::NQ * 4);
-        bulk_copy_g2s(smem_u32(sm + C::Q_OFF + qb * C::Q_BYTES), a.qop + cur.unit * C::Q_BYTES, C::Q_BYTES, qbar);
-        bulk_copy_g2s(smem_u32(&ms.qsig[qb][0]), a.qsig + cur.unit * C::NQ, C::NQ * 4, qbar);
-      }
-      __syncwarp();
-    }
   }
 }
 
@@ -611,8 +605,9 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)
 // A unit split across CTAs: after this CTA's partial (normalised O, LSE) is
 // written, count it.  The CTA that brings the count to the unit's number of
 // parts merges them once its own tiles are done (at most two such units per
-// CTA: the first and the last of its range).  The counters were zeroed by
-// the pre-pass of this launch.
+// CTA: the first and the last of its range).  Every counter is zero when a
+// call starts: the workspace starts zero-filled and the CTA that completes a
+// unit puts its counter back to zero.
 __device__ void count_part(const AttnArgs& a, Misc& ms, int64_t unit) {
   const int64_t u0 = unit * a.tpt;
   const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
@@ -620,8 +615,10 @@ __device__ void count_part(const AttnArgs& a, Misc& ms, int64_t unit) {
   __threadfence();
   named_bar_sync(1, kSmxThreads);
   if (threadIdx.x == 0) {
-    grid_dependency_wait();
-    if (atomicAdd(a.unit_cnt + unit, 1) == c1 - c0) ms.merge_unit[ms.n_merge++] = unit;
+    if (atomicAdd(a.unit_cnt + unit, 1) == c1 - c0) {
+      a.unit_cnt[unit] = 0;              // left at zero for the next call
+      ms.merge_unit[ms.n_merge++] = unit;
+    }
   }
 }
 
@@ -718,9 +715,15 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   int seg = -1;
   bool ok = true;                  // false once a wait gave up: keep going through every barrier
   TileCursor cur(a, b0);
+  QueryBuild<HG, kQ8> qnext;       // the next segment's query, loaded ahead of its build
+  qnext.load(a, cur.t, cur.hgi * a.hg);
+  qnext.template store<C::NQ>(a, sm + C::Q_OFF, ms.qsig[0]);
+  fence_proxy_async_smem();
+  mbar_arrive(smem_u32(&ms.q_full[0]));
   for (int it = 0; it < n_it; ++it, cur.advance(a)) {
     const bool first = cur.first(it), last = cur.last(a, it, n_it);
     const int stage = it % C::NST, pb = it % C::NPB;
+    const bool build_next = last && it + 1 < n_it;      // the next tile starts a new segment
     if (first) {
       ++seg;
       const int qb = seg % C::NQB;
@@ -769,8 +772,12 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       tc_fence_before();
       mbar_arrive(smem_u32(&ms.s_free[sb]));
     }
-    // the segment's query buffer (operand and column multipliers) is no longer needed
-    if (last) mbar_arrive(smem_u32(&ms.q_free[qb]));
+    // the next segment's query: its loads fly while this tile's P is formed
+    if (build_next) {
+      const int nt = cur.hgi + 1 == a.hgs ? cur.t + 1 : cur.t;
+      const int nh0 = cur.hgi + 1 == a.hgs ? 0 : (cur.hgi + 1) * a.hg;
+      qnext.load(a, nt, nh0);
+    }
     if (!valid) {
 #pragma unroll
       for (int h = 0; h < HPT; ++h) s2[h] = -INFINITY;
@@ -879,6 +886,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(smem_u32(&ms.p_full[pb]));
+    // every thread passed this tile's barrier after its last read of the scores'
+    // multipliers, and QK^T of this tile (the last reader of the operand) is done
+    if (build_next) {
+      const int nqb = (seg + 1) % C::NQB;
+      qnext.template store<C::NQ>(a, sm + C::Q_OFF + nqb * C::Q_BYTES, ms.qsig[nqb]);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&ms.q_full[nqb]));
+    }
 
     if (!last) continue;
     // ---- end of a segment: denominators, O normalisation, stores
@@ -969,8 +984,7 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ms.s_full[s]), 1);
       mbar_init(smem_u32(&ms.s_free[s]), kSmxThreads);
-      mbar_init(smem_u32(&ms.q_full[s]), 1);
-      mbar_init(smem_u32(&ms.q_free[s]), kSmxThreads);
+      mbar_init(smem_u32(&ms.q_full[s]), kSmxThreads);
       mbar_init(smem_u32(&ms.p_full[s]), kSmxThreads);
       mbar_init(smem_u32(&ms.pv_done[s]), 1);
     }
@@ -983,14 +997,19 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
     tmem_alloc(smem_u32(&ms.tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
-  // the P operands start zeroed: their padding rows (N rounded up to 16) stay zero
-  for (int i = tid; i < C::NPB * C::P_BYTES / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sm + C::P_OFF)[i] = make_uint4(0, 0, 0, 0);
+  // the query and P operands start zeroed: their padding rows (N rounded up
+  // to 16) stay zero
+  for (int i = tid; i < (C::NQB * C::Q_BYTES + C::NPB * C::P_BYTES) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sm + C::Q_OFF)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < 2 * 64; i += kThreads) (&ms.qsig[0][0])[i] = 0.f;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  // launched as a programmatic dependent: everything above overlapped the
+  // previous kernel in the stream, whose results are visible from here on
+  grid_dependency_wait();
 
   if (warp < kSmxWarps)
     softmax_role<HG, kScaled, kQ8>(a, sm, ms, tmem, b0, n_it, cta);
@@ -1023,8 +1042,8 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
       return;   // the launch below is skipped; the caller sees the attribute error
     configured.fetch_or(bit);
   }
-  // programmatic dependent launch: set-up, index translation and the first
-  // row gathers overlap the query pre-pass; operand reads wait for it
+  // programmatic dependent launch: the set-up (barriers, tensor memory,
+  // zeroed operands) may overlap the tail of the previous kernel
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kThreads);
@@ -1040,9 +1059,6 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
 
 template <int HG>
 void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
-  const unsigned units = (unsigned)((int64_t)a.T * a.hgs);
-  if (q8) prep_query_kernel<HG, true><<<units, 256, 0, stream>>>(a);
-  else prep_query_kernel<HG, false><<<units, 256, 0, stream>>>(a);
   if (q8) launch_tc<HG, false, true>(a, stream);
   else if (a.scaled) launch_tc<HG, true, false>(a, stream);
   else launch_tc<HG, false, false>(a, stream);
