@@ -38,6 +38,7 @@ from sparse_mla_attention_page_gb300 import workloads as W  # noqa: E402
 METRIC = "sparse-attn query-tokens/s and KV-gather HBM GB/s (fraction of GB300 roofline)"
 UNIT = "query-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_tc.cu",
                 "sparse_mla_attention_page_gb300/csrc/tc_ptx.cuh"]
 ATTN_KERNEL = "sparse_attn_tc_kernel (one launch per attention call)"
@@ -323,7 +324,11 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
                      "kernel": ATTN_KERNEL, "algorithmic_bytes_per_call": abytes,
                      "attn_us_per_call": round(attn_mean_s * 1e6, 3),
                      "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
-                     "tensor_tflops": round(attn_flops(w) / attn_mean_s / 1e12, 2)},
+                     "tensor_tflops": round(attn_flops(w) / attn_mean_s / 1e12, 2),
+                     # FP8 dense peak = measured BF16 burst x the nominal FP8/BF16 ratio (2)
+                     "tensor_peak_tflops": round(2.0 * float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), 1),
+                     "tensor_frac": round(attn_flops(w) / attn_mean_s / 1e12
+                                          / (2.0 * float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))), 4)},
         "e2e": {"value": round(world * T * n_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

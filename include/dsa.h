@@ -118,11 +118,10 @@ int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* 
 /* ------------------------------------------------------ sparse attention */
 
 /* Workspace bytes the attention entry points need for (T, H, K) on the
- * current device: split-K partial results and one int32 counter per
- * (token, head group), needed only when a (token, head group) is spread over
- * several SMs.  May be 0.  Pass at least this many bytes, 256-byte aligned,
- * zero-filled before the workspace's first use (cudaMemset); every call
- * leaves the counters at zero again, so a workspace is reused as it is. */
+ * current device: split-K partial results (two FP32 slots of [heads, 512] and
+ * [heads] per SM), needed only when a (token, head group) is spread over
+ * several SMs.  May be 0.  Pass at least this many bytes, 256-byte aligned;
+ * no initialisation is needed: each call writes every byte it reads. */
 size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
 
 /* Sparse MLA decode with BF16 queries over a paged FP8 pool, either layout
@@ -198,11 +197,10 @@ int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int
  *    DSA_NOALLOC_SCRATCH_BYTES is refused with DSA_ERR_WORKSPACE, nothing
  *    launched.
  *  - All calls share the one array, which keeps whatever the last call left
- *    in it.  The only part that must start at zero, the per-(token, head
- *    group) counters, is zero when the library is loaded and every call
- *    leaves it at zero; the partial results are written before they are
- *    read in the same call.  Calls whose work overlaps on the GPU (other
- *    streams, other host threads) race on the array: serialise them. */
+ *    in it; nothing in it needs clearing, because each call writes the
+ *    partial results before it reads them.  Calls whose work overlaps on
+ *    the GPU (other streams, other host threads) race on the array:
+ *    serialise them. */
 int dsa_sparse_attn_decode_noalloc(const void* q_bf16_dev, int T, int H, int D,
                                    const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
                                    const int32_t* page_table_dev, int B, int max_pages, int page_size,

@@ -163,12 +163,11 @@ def dsa_sparse_attn_workspace_bytes(T: int, H: int, K: int) -> int:
 
 
 def workspace_for(T: int, H: int, K: int, device=None) -> torch.Tensor | None:
-    """A zero-filled device workspace of the size the attention entry points
-    need (or None).  Reuse it across calls: each call leaves it ready for the next."""
+    """A device workspace of the size the attention entry points need (or None)."""
     n = dsa_sparse_attn_workspace_bytes(T, H, K)
     if n == 0:
         return None
-    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def _attn_common(q, pool, layout, topk, o, lse, page_table, token_seq, workspace, err_flag):

@@ -123,7 +123,6 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   char* wsb = static_cast<char*>(ws);
   a.ws_o = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_o_offset) : nullptr;
   a.ws_lse = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_lse_offset) : nullptr;
-  a.unit_cnt = plan.split ? reinterpret_cast<int32_t*>(wsb + plan.cnt_offset) : nullptr;
   a.err = err;
   cudaGetLastError();
   dsa::launch_sparse_attn(a, q8, static_cast<cudaStream_t>(stream));

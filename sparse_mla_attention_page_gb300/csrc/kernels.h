@@ -17,8 +17,7 @@ void launch_quantize_q8(const void* q, int64_t n_vec, void* q8, float* scale, in
 // list into tiles of 128 entries: n_tiles = T * hgs * tpt.  The persistent
 // kernel runs `grid` CTAs; CTA c owns the contiguous global tiles
 // [c * n_tiles / grid, (c + 1) * n_tiles / grid).  A unit whose tiles span more
-// than one CTA leaves one partial result per CTA; the CTA that finishes the
-// unit's last part merges them.
+// than one CTA leaves one partial result per CTA, merged by combine_kernel.
 struct AttnArgs {
   const void* q;          // BF16 [T,H,512] or E4M3 [T,H,512]
   const float* q_scale;   // [T,H] for FP8 queries, else nullptr
@@ -39,25 +38,25 @@ struct AttnArgs {
   int grid;
   float* ws_o;            // [grid][2][hg][512] normalised partial O (slot 0: the CTA's first unit)
   float* ws_lse;          // [grid][2][hg]
-  int32_t* unit_cnt;      // [units] parts of a split unit finished so far (zero between calls)
   int32_t* err;
 };
 
 // Launch plan shared by the workspace query and the launch.  Workspace (only
-// when a unit spans two or more CTAs): split-K partials and one counter per
-// unit; the counters must be zero before a workspace's first use and every
-// call leaves them at zero.
+// when a unit spans two or more CTAs): split-K partials, two slots per CTA.
 struct AttnPlan {
   int hg, hgs, tpt;
   int64_t n_tiles;
   int grid;
   bool split;
-  size_t ws_o_offset, ws_lse_offset, cnt_offset;
+  size_t ws_o_offset, ws_lse_offset;
   size_t ws_bytes;
 };
 AttnPlan plan_attn(int T, int H, int K, int sms);
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
+
+// Merges the partial results of split units (after the attention kernel).
+void launch_combine(const AttnArgs& a, cudaStream_t stream);
 
 // Heads handled together by one CTA of the attention kernel.
 int head_group(int H);

@@ -23,7 +23,6 @@ namespace {
 constexpr size_t kScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
-// zero-initialised when the library is loaded (the per-unit counters rely on it)
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;

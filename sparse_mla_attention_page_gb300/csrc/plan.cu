@@ -1,6 +1,6 @@
 // Launch plan and workspace layout of the persistent attention kernel.  Units
 // (token, head group) whose tiles span two or more CTAs leave normalised
-// partial results in the workspace; the last CTA to finish a unit merges them.
+// partial results in the workspace; combine_kernel merges them.
 #include "dsa_common.cuh"
 #include "kernels.h"
 
@@ -16,13 +16,11 @@ AttnPlan plan_attn(int T, int H, int K, int sms) {
   p.grid = (int)(p.n_tiles < sms ? p.n_tiles : sms);
   for (int k = 1; k < p.grid && !p.split; ++k) p.split = tile_begin(k, p.n_tiles, p.grid) % p.tpt != 0;
   auto align = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t units = (size_t)T * p.hgs;
   size_t end = 0;
   if (p.split) {
     p.ws_o_offset = 0;
     p.ws_lse_offset = align(p.ws_o_offset + (size_t)p.grid * 2 * p.hg * kD * sizeof(float));
-    p.cnt_offset = align(p.ws_lse_offset + (size_t)p.grid * 2 * p.hg * sizeof(float));
-    end = p.cnt_offset + units * sizeof(int32_t);
+    end = p.ws_lse_offset + (size_t)p.grid * 2 * p.hg * sizeof(float);
   }
   p.ws_bytes = end;
   return p;

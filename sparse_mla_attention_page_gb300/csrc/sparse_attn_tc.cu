@@ -37,7 +37,10 @@
 //              128 rows, keep a lazy running max (O in TMEM is rescaled only
 //              when the max grows by more than 2^8), form p = 2^(s - m),
 //              accumulate the denominators, write P as an FP8 operand, and at
-//              the end of a segment normalise O and store it.
+//              the end of a segment normalise O and store it (a unit whose
+//              tiles span CTAs leaves a normalised partial O and LSE per CTA;
+//              combine_kernel, launched right behind as a programmatic
+//              dependent, merges them).
 //
 // Exact FP8 operands for BF16 data: a BF16 query q is split per head into
 // hi = e4m3(q * 2^a) and lo = e4m3((q * 2^a - hi) * 16) with a power-of-two
@@ -101,8 +104,6 @@ struct Misc {
   float red2[2][4][16];       // [head half][lane quarter][head] denominators (epilogue)
   __align__(16) float qsig[2][64];   // log2-domain multiplier of each score column, per query buffer
   float linv[32], lse2[32];
-  int64_t merge_unit[2];
-  int n_merge;
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
 static_assert(offsetof(Misc, ring) % 16 == 0 && offsetof(Misc, qsig) % 16 == 0, "vector access alignment");
@@ -602,102 +603,6 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)
   }
 }
 
-// A unit split across CTAs: after this CTA's partial (normalised O, LSE) is
-// written, count it.  The CTA that brings the count to the unit's number of
-// parts merges them once its own tiles are done (at most two such units per
-// CTA: the first and the last of its range).  Every counter is zero when a
-// call starts: the workspace starts zero-filled and the CTA that completes a
-// unit puts its counter back to zero.
-__device__ void count_part(const AttnArgs& a, Misc& ms, int64_t unit) {
-  const int64_t u0 = unit * a.tpt;
-  const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
-  const int c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
-  __threadfence();
-  named_bar_sync(1, kSmxThreads);
-  if (threadIdx.x == 0) {
-    if (atomicAdd(a.unit_cnt + unit, 1) == c1 - c0) {
-      a.unit_cnt[unit] = 0;              // left at zero for the next call
-      ms.merge_unit[ms.n_merge++] = unit;
-    }
-  }
-}
-
-// LSE = logsumexp_c LSE_c and O = sum_c exp(LSE_c - LSE) O_c over the CTAs c
-// holding part of the unit, folded part by part with a running maximum.
-// Each thread owns 4 dims (d4) of heads hq, hq + 2, ...; the loads of a
-// batch of parts and heads are all issued before any is used, so a merge
-// costs about one L2 round trip per batch instead of one per part and head.
-template <int HG>
-__device__ void merge_unit(const AttnArgs& a, int64_t unit) {
-  const int64_t u0 = unit * a.tpt;
-  const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
-  const int c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
-  const int t = (int)(unit / a.hgs), h0 = (int)(unit - (int64_t)t * a.hgs) * a.hg;
-  const int tid = threadIdx.x;
-  const int d4 = tid & (kD / 4 - 1), hq = tid >> 7;
-  constexpr int kPer = HG / 2;                 // heads per thread
-  constexpr int kChunk = kPer < 8 ? kPer : 8;  // heads per batch
-  constexpr int kParts = 2;                    // parts per batch
-#pragma unroll 1
-  for (int j0 = 0; j0 < kPer; j0 += kChunk) {
-    float m[kChunk], sum[kChunk];
-    float4 acc[kChunk];
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      m[j] = -INFINITY;
-      sum[j] = 0.f;
-      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll 1
-    for (int cb = c0; cb <= c1; cb += kParts) {
-      float ls[kParts][kChunk];
-      float4 v[kParts][kChunk];
-#pragma unroll
-      for (int pp = 0; pp < kParts; ++pp) {
-        const int c = cb + pp;
-        const bool have = c <= c1;
-        const int64_t sb = ((int64_t)c * 2 + (have && tile_begin(c, a.n_tiles, a.grid) < u0 ? 1 : 0)) * a.hg;
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          const int h = hq + 2 * (j0 + j);
-          ls[pp][j] = have ? __ldcg(a.ws_lse + sb + h) : -INFINITY;
-          v[pp][j] = have ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + (sb + h) * kD) + d4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int pp = 0; pp < kParts; ++pp) {
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          if (ls[pp][j] == -INFINITY) continue;          // a part with no valid entry adds nothing
-          const float mn = fmaxf(m[j], ls[pp][j]);
-          const float r = expf(m[j] - mn);               // 0 while m is -inf
-          const float w = expf(ls[pp][j] - mn);
-          sum[j] = sum[j] * r + w;
-          acc[j].x = fmaf(w, v[pp][j].x, acc[j].x * r);
-          acc[j].y = fmaf(w, v[pp][j].y, acc[j].y * r);
-          acc[j].z = fmaf(w, v[pp][j].z, acc[j].z * r);
-          acc[j].w = fmaf(w, v[pp][j].w, acc[j].w * r);
-          m[j] = mn;
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const int h = hq + 2 * (j0 + j);
-      const float inv = sum[j] > 0.f ? 1.f / sum[j] : 0.f;
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
-      uint2 packed;
-      packed.x = *reinterpret_cast<uint32_t*>(&lo);
-      packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      const int64_t th = (int64_t)t * a.H + h0 + h;
-      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + th * kD)[d4] = packed;
-      if (d4 == 0) a.lse[th] = sum[j] > 0.f ? m[j] + logf(sum[j]) : -INFINITY;
-    }
-  }
-}
-
 template <int HG, bool kScaled, bool kQ8>
 __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it,
                              int cta) {
@@ -947,14 +852,6 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       if (whole) a.lse[(int64_t)cur.t * a.H + h0 + h] = lse;
       else a.ws_lse[slot * a.hg + h] = lse;
     }
-    if (!whole) count_part(a, ms, cur.unit);
-  }
-  // units whose last part this CTA finished: merge them now that its own tiles are done
-  if (a.unit_cnt != nullptr) {
-    named_bar_sync(1, kSmxThreads);
-    const int n_merge = ms.n_merge;
-    if (n_merge > 0) __threadfence();
-    for (int i = 0; i < n_merge; ++i) merge_unit<HG>(a, ms.merge_unit[i]);
   }
   (void)ok;
 }
@@ -990,7 +887,6 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
     }
     mbar_init(smem_u32(&ms.mma_final), 1);
     ms.abort = 0;
-    ms.n_merge = 0;
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -1010,6 +906,9 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
   // launched as a programmatic dependent: everything above overlapped the
   // previous kernel in the stream, whose results are visible from here on
   grid_dependency_wait();
+  // the split-unit merge may be scheduled now: its blocks take SMs as CTAs
+  // of this grid exit and wait for the whole grid before reading partials
+  grid_launch_dependents();
 
   if (warp < kSmxWarps)
     softmax_role<HG, kScaled, kQ8>(a, sm, ms, tmem, b0, n_it, cta);
@@ -1062,6 +961,7 @@ void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
   if (q8) launch_tc<HG, false, true>(a, stream);
   else if (a.scaled) launch_tc<HG, true, false>(a, stream);
   else launch_tc<HG, false, false>(a, stream);
+  if (a.ws_o != nullptr) launch_combine(a, stream);
 }
 
 }  // namespace

@@ -63,20 +63,14 @@ def test_noalloc_matches_workspace_entry_point_twice():
         _close(o, lse, o_ref, lse_ref)
 
 
-def test_noalloc_refuses_workspace_beyond_limit():
+def test_noalloc_array_covers_every_shape():
+    """The split-K workspace holds two partial slots per SM, whatever T and K
+    are, so on this GPU the static array serves every supported shape; a
+    shape that did not fit would be refused with DSA_ERR_WORKSPACE before
+    any launch."""
     build_mod.build()
-    shape = None
-    for T in (1, 64, 4096, 1 << 18, 1 << 20, 1 << 22):
-        for K in (2048, 16384):
-            if binding.dsa_sparse_attn_workspace_bytes(T, 128, K) > (32 << 20):
-                shape = (T, 128, K)
-                break
-        if shape:
-            break
-    if shape is None:
-        pytest.skip("the split plan never needs more than the static array for these shapes")
-    T, H, K = shape
-    fake = 0x10000          # aligned, never dereferenced: the call must refuse before launching
-    st = binding.lib().dsa_sparse_attn_decode_noalloc(fake, T, H, 512, fake, 4096, 0, 512, None, 1, 1, 64,
-                                                      None, fake, K, 0.1, fake, fake, None, None)
-    assert st == 7          # DSA_ERR_WORKSPACE
+    limit = 32 << 20
+    for H in (8, 16, 32, 64, 128):
+        for T in (1, 64, 4096, 1 << 20):
+            for K in (128, 2048, 65536):
+                assert binding.dsa_sparse_attn_workspace_bytes(T, H, K) <= limit, (T, H, K)
