@@ -81,7 +81,7 @@ def algorithmic_bytes(w: dict) -> int:
     T, H, K = w["T"], w["H"], w["K"]
     R = 512 if w["layout"] == "raw512" else 528
     valid = W.valid_entry_count(w["topk"])
-    q8 = w["name"] == "prefill_q8_raw512"
+    q8 = w["name"].startswith("prefill_q8")
     q_bytes = T * H * 512 * (1 if q8 else 2) + (T * H * 4 if q8 else 0)
     return valid * R + q_bytes + T * K * 4 + T * H * 512 * 2 + T * H * 4
 
@@ -181,7 +181,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     w = make_workload(args.workload)
     T, H, K = w["T"], w["H"], w["K"]
     layout = w["layout"]
-    prefill = w["name"] == "prefill_q8_raw512"
+    prefill = w["name"].startswith("prefill_q8")
 
     def to_dev(a, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(a))
@@ -355,7 +355,7 @@ def oracle_setup(w: dict):
     import oracle
     pool = oracle.fill_pool(w)
     q8 = qs = None
-    if w["name"] == "prefill_q8_raw512":
+    if w["name"].startswith("prefill_q8"):
         q8, qs = oracle.quantize_q8(w["q_bf16"])
     return pool, q8, qs
 
@@ -369,7 +369,7 @@ def cpu_baseline(w: dict, seconds: float) -> dict:
     pool, q8, qs = oracle_setup(w)
     x_new, slots = step_rows(w)
     T = w["T"]
-    tokens = np.arange(min(T, 64)) if w["name"] == "prefill_q8_raw512" else np.arange(T)
+    tokens = np.arange(min(T, 64)) if w["name"].startswith("prefill_q8") else np.arange(T)
     done = 0
     t0 = time.perf_counter()
     while True:

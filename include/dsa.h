@@ -159,10 +159,13 @@ int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D,
                            void* stream);
 
 /* Sparse MLA prefill with FP8 queries ("Q8", [P3 Modifications]): the same
- * definition with q[t][h][d] = e4m3(q8[t][h][d]) * q_scale[t][h].  Only the
- * raw 512-byte layout is accepted: a group-scaled pool is refused with
- * DSA_ERR_LAYOUT, as the pages keep Q8 away from packed/scaled FP8 rows
- * [P3 review thread: the packed-FP8 KPool guard].
+ * definition with q[t][h][d] = e4m3(q8[t][h][d]) * q_scale[t][h].  Both row
+ * layouts are accepted.  The pages' Q8 prefill stops at raw rows and guards
+ * against packed FP8 pools [P3 review thread: the packed-FP8 KPool guard;
+ * "[DSA] Support group-scaled FP8 NoPE KV reads for CUDA TileLang",
+ * Modifications: native FP8 attention over the scaled layout not included];
+ * over 528-byte rows this library applies each group's scale exactly as the
+ * BF16-query decode does.
  *   q8_dev       [T, H, 512] E4M3 bytes, 16-byte aligned.
  *   q_scale_dev  [T, H] float. */
 int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int T, int H, int D,

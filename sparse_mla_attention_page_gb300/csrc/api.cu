@@ -74,7 +74,6 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   if (T < 0 || pool_rows < 0) return DSA_ERR_SHAPE;
   if (D != 512 || kv_row_dim != 512) return DSA_ERR_ROW_WIDTH;
   if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528) return DSA_ERR_LAYOUT;
-  if (q8 && layout != DSA_KV_RAW512) return DSA_ERR_LAYOUT;
   if (K <= 0 || K % 128 != 0) return DSA_ERR_TOPK_PAD;
   if (!heads_ok(H)) return DSA_ERR_HEADS;
   if (T == 0) return DSA_OK;

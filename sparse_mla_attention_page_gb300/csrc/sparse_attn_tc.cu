@@ -958,7 +958,8 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
 
 template <int HG>
 void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
-  if (q8) launch_tc<HG, false, true>(a, stream);
+  if (q8 && a.scaled) launch_tc<HG, true, true>(a, stream);
+  else if (q8) launch_tc<HG, false, true>(a, stream);
   else if (a.scaled) launch_tc<HG, true, false>(a, stream);
   else launch_tc<HG, false, false>(a, stream);
   if (a.ws_o != nullptr) launch_combine(a, stream);

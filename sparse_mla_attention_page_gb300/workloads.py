@@ -21,6 +21,9 @@ Workloads (all 512-dim NoPE latent rows, page size 64, sm_scale = 1/sqrt(576)):
   context rows of one sequence, 32 heads, 16384-row pool; token at position
   p draws min(2048, 8193 + p) distinct causal indices from [0, 8192 + p],
   padded to a multiple of 128 with -1.
+* ``prefill_q8_scaled528`` the same prefill batch over group-scaled 528-byte
+  rows of N(0,1)*U(0.1,4) (one multiplier per row): FP8 queries over scaled
+  rows, which the pages leave out.
 * ``writer_sweep``         16384 new rows of N(0,1)*U(0.1,8) written to
   distinct random slots of a 262144-row pool; decode over the written slots
   (physical indices, no page table) at 8/16/32 heads, top-k 2048, with one
@@ -44,6 +47,7 @@ WORKLOADS = (
     "decode_raw512",
     "decode_scaled528",
     "prefill_q8_raw512",
+    "prefill_q8_scaled528",
     "writer_sweep",
 )
 
@@ -157,6 +161,18 @@ def prefill_q8_raw512(seed: int = 4, T: int = 4096, H: int = 32, K: int = 2048,
                 token_seq=None, topk=topk, sm_scale=SM_SCALE)
 
 
+def prefill_q8_scaled528(seed: int = 6, T: int = 4096, H: int = 32, K: int = 2048,
+                         context: int = 8192, pool_rows: int = 16384, first_pos: int = 0) -> dict:
+    """The prefill batch over group-scaled 528-byte rows of N(0,1) * U(0.1, 4) per row."""
+    w = prefill_q8_raw512(seed=seed, T=T, H=H, K=K, context=context, pool_rows=pool_rows,
+                          first_pos=first_pos)
+    rng = rng_for(seed + 1000)
+    mult = rng.uniform(0.1, 4.0, size=(pool_rows, 1)).astype(np.float32)
+    kv = rng.standard_normal((pool_rows, D_LATENT), dtype=np.float32) * mult
+    w.update(name="prefill_q8_scaled528", layout="scaled528", kv_src=f32_to_bf16_bits(kv))
+    return w
+
+
 def writer_rows(seed: int = 5, n_rows: int = 16384, pool_rows: int = 262144,
                 mult_hi: float = 8.0) -> dict:
     """New BF16 rows N(0,1)*U(0.1, mult_hi) and distinct random destination slots."""
@@ -192,6 +208,7 @@ def make(name: str, **kw) -> dict:
         "decode_raw512": decode_raw512,
         "decode_scaled528": decode_scaled528,
         "prefill_q8_raw512": prefill_q8_raw512,
+        "prefill_q8_scaled528": prefill_q8_scaled528,
         "writer_sweep": writer_sweep,
     }[name]
     return fn(**kw)

@@ -80,7 +80,7 @@ def test_decode_host_validation(L, kw, code):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(layout=1), 3), (dict(qs=None), 1), (dict(D=1024), 4), (dict(K=64), 5), (dict(H=7), 6),
+    (dict(layout=2), 3), (dict(layout=-1), 3), (dict(qs=None), 1), (dict(D=1024), 4), (dict(K=64), 5), (dict(H=7), 6),
 ])
 def test_prefill_host_validation(L, kw, code):
     assert prefill(L, **kw) == code

@@ -90,6 +90,23 @@ def test_prefill_q8_raw512(T, full):
     assert_attn_close(O, L, Or, Lr, f"prefill_q8 T={T}")
 
 
+@pytest.mark.parametrize("T,full", [(64, True), (4096, False)])
+def test_prefill_q8_scaled528(T, full):
+    """FP8 queries over group-scaled 528-byte rows (beyond the pages, which keep
+    Q8 prefill to raw rows): the same definition, scales applied per group."""
+    w = W.prefill_q8_scaled528(T=T)
+    pool, pd = pool_for(w, ("prefill_scaled", T))
+    q8, qs = oracle.quantize_q8(w["q_bf16"])
+    O, L, err = run_prefill(w, pd, q8, qs)
+    tok = None if full else sample_tokens(T, 24, 9)
+    Or, Lr, _ = oracle.sparse_attn(pool, "scaled528", w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                                   page_table=w["page_table"], tokens=tok)
+    assert err == 0
+    if tok is not None:
+        O, L = O[tok], L[tok]
+    assert_attn_close(O, L, Or, Lr, f"prefill_q8_scaled528 T={T}")
+
+
 def test_prefill_q8_short_context_padding():
     """Zero prior context: early tokens have fewer than K causal rows, so the
     list is padded with -1 (down to a single valid entry for the first token)."""
