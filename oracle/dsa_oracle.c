@@ -384,6 +384,54 @@ int oracle_sparse_attn(int q_kind, const void* q, const float* q_scale, int T, i
   return J.err;
 }
 
+/* ------------------------------------------------ gather / dequantise reader */
+
+/* BF16 bits of a finite float, rounded to nearest, ties to even. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* The rows a top-k list selects, dequantised to BF16, in one padded buffer
+ * ("[DSA] Support group-scaled FP8 NoPE KV reads for CUDA TileLang",
+ * Modifications: the gather/cast reader that feeds BF16 consumers; pull 44217,
+ * review thread: the paged gather with -1 padding).  For entry j of token t,
+ * slot e = t*K + j:
+ *   out[e][d] = bf16_rne( fp32( e4m3(b_d) * s_g ) )  (raw rows: s = 1, exact),
+ *   idx_out[e] = e for a valid entry, -1 for a masked one (its out row is
+ *   left as it is).  Rows resolve as in the attention (same error bits).
+ * The FP32 product is formed once (the exact product fits a double; the cast
+ * rounds it to nearest FP32), then rounded to BF16. */
+int oracle_gather_dequant(const uint8_t* pool, int64_t pool_rows, int layout,
+                          const int32_t* page_table, int B, int max_pages, int page_size,
+                          const int32_t* token_seq, const int32_t* topk, int T, int K,
+                          uint16_t* out, int32_t* idx_out) {
+  attn_job J;
+  memset(&J, 0, sizeof J);
+  J.pool = pool; J.pool_rows = pool_rows; J.layout = layout;
+  J.page_table = page_table; J.B = B; J.max_pages = max_pages; J.page_size = page_size;
+  J.token_seq = token_seq;
+  int err = 0;
+  const int64_t R = layout == 0 ? 512 : 528;
+  for (int t = 0; t < T; ++t) {
+    for (int j = 0; j < K; ++j) {
+      const int64_t e = (int64_t)t * K + j;
+      const int64_t row = resolve_row(&J, t, topk[e], &err);
+      idx_out[e] = row < 0 ? -1 : (int32_t)e;
+      if (row < 0) continue;
+      const uint8_t* r = pool + row * R;
+      for (int d = 0; d < ORACLE_D; ++d) {
+        double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * (d / ORACLE_GROUP));
+        float v = (float)(oracle_e4m3_decode(r[d]) * s);
+        out[e * ORACLE_D + d] = f32_to_bf16_rne(v);
+      }
+    }
+  }
+  return err;
+}
+
 /* ------------------------------------------------------- array conveniences */
 
 void oracle_e4m3_encode_array(const float* x, int64_t n, uint8_t* out, int bruteforce) {

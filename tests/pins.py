@@ -391,9 +391,42 @@ def pin_wrong_index_is_detected():
     assert (diff > 0).any()
 
 
+def pin_gather_dequant_torch():
+    """The reader's BF16 rows are PyTorch's own FP8 decode (raw rows, exact in
+    BF16) and PyTorch's FP32 product with the group scale cast to BF16 (scaled
+    rows); its remapped indices are the slot numbers, -1 where masked; an
+    entry outside the page table is masked with the same error bit as the
+    attention."""
+    for layout, seed, seqs in (("raw512", 81, 1), ("scaled528", 82, 2)):
+        w, pool = _tiny(layout, seed, T=4, K=128, seqs=seqs)
+        topk = w["topk"].copy()
+        out, idx, err = oracle.gather_dequant(pool, layout, topk, page_table=w["page_table"],
+                                              page_size=64, token_seq=w["token_seq"])
+        assert err == 0
+        T, K = topk.shape
+        want_idx = np.where(topk >= 0, np.arange(T * K, dtype=np.int32).reshape(T, K), -1)
+        np.testing.assert_array_equal(idx, want_idx)
+        e = np.nonzero(topk.reshape(-1) >= 0)[0]
+        rows = np.array([_phys(w["page_table"], w["token_seq"], int(i) // K, int(topk.reshape(-1)[i]))
+                         for i in e])
+        r = torch.from_numpy(np.ascontiguousarray(pool[rows, :512])).view(torch.float8_e4m3fn)
+        if layout == "raw512":
+            want = r.to(torch.bfloat16)
+        else:
+            sc = torch.from_numpy(np.ascontiguousarray(pool[rows, 512:]).view("<f4").copy())
+            want = (r.to(torch.float32) * sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
+        np.testing.assert_array_equal(out[e], want.view(torch.int16).numpy().view(np.uint16))
+    bad = topk.copy()
+    bad[0, 0] = w["page_table"].shape[1] * 64 + 1          # beyond the page table's width
+    _, idx2, err2 = oracle.gather_dequant(pool, "scaled528", bad, page_table=w["page_table"],
+                                          page_size=64, token_seq=w["token_seq"])
+    assert err2 == oracle.ERR_INDEX_RANGE and idx2[0, 0] == -1
+
+
 ALL_PINS = [
     pin_decode_spec, pin_decode_torch, pin_encode_exhaustive_bf16, pin_encode_ties_and_f32,
     pin_encode_roundtrip, pin_scaled_worked_example, pin_raw_writer_torch,
     pin_scaled_writer_invariants, pin_attn_sdpa, pin_attn_closed_forms, pin_attn_invariances,
     pin_q8_matches_bf16_decode, pin_q8_quantiser, pin_error_bits, pin_wrong_index_is_detected,
+    pin_gather_dequant_torch,
 ]

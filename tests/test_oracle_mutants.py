@@ -40,6 +40,10 @@ MUTANTS = {
                    "    float s = amax / 512.0f;\n    for (int j = 0; j < d; ++j) q8"),
     "index_range_unchecked": ("if (page >= J->max_pages) { *err |= ORACLE_ERR_INDEX_RANGE; return -1; }",
                               "if (page >= J->max_pages) { return -1; }"),
+    "reader_bf16_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;"),
+    "reader_scale_group": ("double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * (d / ORACLE_GROUP));",
+                           "double s = layout == 0 ? 1.0 : (double)le_f32(r + 512);"),
+    "reader_index_not_remapped": ("idx_out[e] = row < 0 ? -1 : (int32_t)e;", "idx_out[e] = row < 0 ? -1 : topk[e];"),
 }
 
 
