@@ -423,7 +423,8 @@ int oracle_gather_dequant(const uint8_t* pool, int64_t pool_rows, int layout,
       if (row < 0) continue;
       const uint8_t* r = pool + row * R;
       for (int d = 0; d < ORACLE_D; ++d) {
-        double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * (d / ORACLE_GROUP));
+        const int g = d / ORACLE_GROUP;                 /* the 128-dim group of d */
+        double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * g);
         float v = (float)(oracle_e4m3_decode(r[d]) * s);
         out[e * ORACLE_D + d] = f32_to_bf16_rne(v);
       }

@@ -41,8 +41,7 @@ MUTANTS = {
     "index_range_unchecked": ("if (page >= J->max_pages) { *err |= ORACLE_ERR_INDEX_RANGE; return -1; }",
                               "if (page >= J->max_pages) { return -1; }"),
     "reader_bf16_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;"),
-    "reader_scale_group": ("double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * (d / ORACLE_GROUP));",
-                           "double s = layout == 0 ? 1.0 : (double)le_f32(r + 512);"),
+    "reader_scale_group": ("const int g = d / ORACLE_GROUP;", "const int g = d % 4;"),
     "reader_index_not_remapped": ("idx_out[e] = row < 0 ? -1 : (int32_t)e;", "idx_out[e] = row < 0 ? -1 : topk[e];"),
 }
 
