@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--op", choices=["attention", "gather_dequant"], default="attention",
+                   help="gather_dequant times the BF16 reader over the workload's top-k lists instead")
     return p.parse_args()
 
 
@@ -88,6 +90,54 @@ def algorithmic_bytes(w: dict) -> int:
 
 def attn_flops(w: dict) -> int:
     return 4 * w["H"] * 512 * W.valid_entry_count(w["topk"])
+
+
+def run_gather(args) -> dict:
+    """The gather/dequantise reader over the workload's pool and top-k lists:
+    CUDA events around each call, L2 flushed before every call."""
+    import torch
+
+    from sparse_mla_attention_page_gb300 import binding
+    dev = torch.device("cuda", 0)
+    w = make_workload(args.workload)
+    T, K, layout = w["T"], w["K"], w["layout"]
+    R = 512 if layout == "raw512" else 528
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    pool = torch.zeros(w["pool_rows"], R, dtype=torch.uint8, device=dev)
+    (binding.dsa_kv_write_raw if layout == "raw512" else binding.dsa_kv_write_scaled)(
+        bf(w["kv_src"]), torch.from_numpy(w["kv_slots"]).to(dev), pool)
+    topk = torch.from_numpy(w["topk"]).to(dev)
+    pt = None if w["page_table"] is None else torch.from_numpy(w["page_table"]).to(dev)
+    out = torch.empty(T * K, 512, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 256 << 20),
+                        dtype=torch.uint8, device=dev)
+    call = lambda: binding.dsa_gather_dequant(pool, layout, topk, out, idx, page_table=pt,  # noqa: E731
+                                              page_size=w["page_size"])
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize(dev)
+    us = float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) * 1e3
+    valid = W.valid_entry_count(w["topk"])
+    abytes = valid * R + valid * 1024 + T * K * 8
+    peak = float(measured_peaks().get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = abytes / (us * 1e-6) / 1e9
+    return {"metric": "gather-dequant selected rows/s and HBM GB/s (fraction of GB300 roofline)",
+            "value": round(valid / (us * 1e-6), 1), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "us_per_call": round(us, 3), "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "op": "gather_dequant", "T": T, "K": K, "layout": layout,
+                       "valid_entries": valid, "l2": "flushed before every call"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "algorithmic_bytes_per_call": abytes}}
 
 
 def measured_peaks() -> dict:
@@ -436,6 +486,10 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     import importlib
     importlib.import_module("sparse_mla_attention_page_gb300.build").build()
+    if args.op == "gather_dequant":
+        if rank == 0:
+            print(json.dumps(run_gather(args)), flush=True)
+        return
     out = run_ours(args, rank, world, local_rank, dist)
     if out is not None:
         line, w = out

@@ -176,6 +176,29 @@ int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int
                                void* workspace_dev, size_t ws_bytes, int32_t* err_flag_dev,
                                void* stream);
 
+/* ------------------------------------------- gather / dequantise reader */
+
+/* The rows a top-k list selects, dequantised to BF16 in a buffer padded to
+ * one slot per top-k entry, for consumers that attend in BF16 ["[DSA] Support
+ * group-scaled FP8 NoPE KV reads for CUDA TileLang", Modifications: the
+ * gather/cast reader; P3 review thread: the paged gather with -1 padding].
+ * For slot e = t*K + j of entry j of token t:
+ *   out[e][d]  = bf16_rn(fp32(e4m3(b_d) * s_g))   (raw rows: s = 1, exact),
+ *   idx_out[e] = e for a valid entry, -1 for a masked one (out[e] untouched).
+ * Rows resolve exactly as in the attention (page table, token_seq, -1
+ * sentinels, the same error bits in err_flag_dev).
+ *   pool_dev        [pool_rows, 512 or 528] bytes, 16-byte aligned.
+ *   page_table_dev  [B, max_pages] int32, or NULL (indices are physical rows).
+ *   token_seq_dev   [T] int32 or NULL.
+ *   topk_dev        [T, K] int32, any K >= 1, T * K < 2^31.
+ *   out_bf16_dev    [T * K, 512] BF16, 16-byte aligned.
+ *   idx_out_dev     [T, K] int32.
+ * T == 0 is a no-op. */
+int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
+                       const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                       const int32_t* token_seq_dev, const int32_t* topk_dev, int T, int K,
+                       void* out_bf16_dev, int32_t* idx_out_dev, int32_t* err_flag_dev, void* stream);
+
 /* ------------------------------------------- decode without allocation */
 
 /* Largest split-K workspace dsa_sparse_attn_decode_noalloc can serve (32 MiB). */

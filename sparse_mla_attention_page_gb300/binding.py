@@ -33,7 +33,7 @@ _lib = None
 EXPORTS = (
     "dsa_status_string", "dsa_kv_row_bytes", "dsa_kv_write_raw", "dsa_kv_write_scaled",
     "dsa_quantize_q8", "dsa_sparse_attn_workspace_bytes", "dsa_sparse_attn_decode",
-    "dsa_sparse_attn_prefill_q8", "dsa_sparse_attn_decode_noalloc",
+    "dsa_sparse_attn_prefill_q8", "dsa_gather_dequant", "dsa_sparse_attn_decode_noalloc",
 )
 
 
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
             L.dsa_sparse_attn_prefill_q8.argtypes = [
                 vp, vp, i32, i32, i32, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i32,
                 c.c_float, vp, vp, vp, c.c_size_t, vp, vp]
+            L.dsa_gather_dequant.restype = i32
+            L.dsa_gather_dequant.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp]
             L.dsa_sparse_attn_decode_noalloc.restype = i32
             L.dsa_sparse_attn_decode_noalloc.argtypes = [
                 vp, i32, i32, i32, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i32,
@@ -192,6 +194,34 @@ def _attn_common(q, pool, layout, topk, o, lse, page_table, token_seq, workspace
         _need(err_flag, "err_flag", torch.int32)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return T, H, lay, B, max_pages, ws_bytes
+
+
+def dsa_gather_dequant(pool, layout, topk, out, idx_out, page_table=None, page_size=64,
+                       token_seq=None, err_flag=None, stream=None) -> None:
+    """BF16 rows out [T*K, 512] and remapped indices idx_out [T, K] for topk [T, K]."""
+    _need(pool, "pool", torch.uint8)
+    _need(topk, "topk", torch.int32)
+    _need(out, "out", torch.bfloat16, 512)
+    _need(idx_out, "idx_out", torch.int32)
+    if topk.dim() != 2:
+        raise ValueError("topk must be [T, K] int32")
+    T, K = topk.shape
+    if out.shape[0] < T * K or tuple(idx_out.shape) != (T, K):
+        raise ValueError("out must be [T*K, 512] bf16 and idx_out [T, K] int32")
+    lay = LAYOUTS.get(layout, layout)
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32)
+        B, max_pages = page_table.shape
+    else:
+        B, max_pages = 1, 1
+    if token_seq is not None:
+        _need(token_seq, "token_seq", torch.int32)
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32)
+    _check(lib().dsa_gather_dequant(_ptr(pool), pool.shape[0], lay, _ptr(page_table), B, max_pages,
+                                    page_size, _ptr(token_seq), _ptr(topk), T, K, _ptr(out),
+                                    _ptr(idx_out), _ptr(err_flag), _stream(stream)),
+           "dsa_gather_dequant")
 
 
 def _kv_row_dim(pool, lay) -> int:

@@ -180,6 +180,46 @@ int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* 
   return launch_status();
 }
 
+int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
+                       const int32_t* page_table_dev, int B, int max_pages, int page_size,
+                       const int32_t* token_seq_dev, const int32_t* topk_dev, int T, int K,
+                       void* out_bf16_dev, int32_t* idx_out_dev, int32_t* err_flag_dev, void* stream) {
+  if (T < 0 || K < 1 || pool_rows < 0) return DSA_ERR_SHAPE;
+  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528) return DSA_ERR_LAYOUT;
+  if (T == 0) return DSA_OK;
+  if (pool_dev == nullptr || topk_dev == nullptr || out_bf16_dev == nullptr || idx_out_dev == nullptr)
+    return DSA_ERR_NULL;
+  if (pool_rows < 1 || pool_rows > INT32_MAX || (int64_t)T * K > INT32_MAX) return DSA_ERR_SHAPE;
+  if (page_table_dev != nullptr) {
+    if (B < 1 || max_pages < 1 || page_size < 1) return DSA_ERR_SHAPE;
+    if ((int64_t)max_pages * page_size > (int64_t)INT32_MAX + 1) return DSA_ERR_SHAPE;
+  }
+  if (!aligned(pool_dev, 16) || !aligned(out_bf16_dev, 16) || !aligned(topk_dev, 4) ||
+      !aligned(idx_out_dev, 4))
+    return DSA_ERR_ALIGN;
+  int sms = 0;
+  int st = current_device_sms(&sms);
+  if (st != DSA_OK) return st;
+  dsa::GatherArgs g{};
+  g.pool = static_cast<const uint8_t*>(pool_dev);
+  g.pool_rows = pool_rows;
+  g.scaled = layout == DSA_KV_SCALED528;
+  g.page_table = page_table_dev;
+  g.B = B;
+  g.max_pages = max_pages;
+  g.page_size = page_table_dev ? page_size : 1;
+  g.token_seq = page_table_dev ? token_seq_dev : nullptr;
+  g.topk = topk_dev;
+  g.T = T;
+  g.K = K;
+  g.out = out_bf16_dev;
+  g.idx_out = idx_out_dev;
+  g.err = err_flag_dev;
+  cudaGetLastError();
+  dsa::launch_gather_dequant(g, sms, static_cast<cudaStream_t>(stream));
+  return launch_status();
+}
+
 size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K) {
   int sms = 0;
   if (current_device_sms(&sms) != DSA_OK) sms = 152;

@@ -55,6 +55,22 @@ AttnPlan plan_attn(int T, int H, int K, int sms);
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
 
+// Gather / dequantise reader (see gather_dequant.cu).
+struct GatherArgs {
+  const uint8_t* pool;
+  int64_t pool_rows;
+  bool scaled;            // 528-byte rows
+  const int32_t* page_table;
+  int B, max_pages, page_size;
+  const int32_t* token_seq;
+  const int32_t* topk;    // [T, K]
+  int T, K;
+  void* out;              // BF16 [T*K, 512]
+  int32_t* idx_out;       // [T, K]
+  int32_t* err;
+};
+void launch_gather_dequant(const GatherArgs& g, int sms, cudaStream_t stream);
+
 // Merges the partial results of split units (after the attention kernel).
 void launch_combine(const AttnArgs& a, cudaStream_t stream);
 

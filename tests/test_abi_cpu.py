@@ -86,6 +86,24 @@ def test_prefill_host_validation(L, kw, code):
     assert prefill(L, **kw) == code
 
 
+def gather(L, **kw):
+    a = dict(pool=FAKE, rows=4096, layout=0, pt=None, B=1, mp=64, ps=64, ts=None, topk=FAKE, T=4, K=100,
+             out=FAKE, idx=FAKE, err=None)
+    a.update(kw)
+    return L.dsa_gather_dequant(a["pool"], a["rows"], a["layout"], a["pt"], a["B"], a["mp"], a["ps"], a["ts"],
+                                a["topk"], a["T"], a["K"], a["out"], a["idx"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), 2), (dict(K=0), 2), (dict(layout=5), 3), (dict(T=0), 0), (dict(pool=None), 1),
+    (dict(topk=None), 1), (dict(out=None), 1), (dict(idx=None), 1), (dict(rows=0), 2),
+    (dict(T=1 << 20, K=4096), 2), (dict(pt=FAKE, B=0), 2), (dict(pool=FAKE + 4), 10),
+    (dict(out=FAKE + 8), 10), (dict(topk=FAKE + 2), 10),
+])
+def test_gather_host_validation(L, kw, code):
+    assert gather(L, **kw) == code
+
+
 def test_writer_host_validation(L):
     assert L.dsa_kv_write_raw(None, 0, None, None, 10, None, None) == 0          # empty: no-op
     assert L.dsa_kv_write_raw(None, 4, None, None, 10, None, None) == 1
