@@ -40,8 +40,9 @@ UNIT = "query-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_tc.cu",
-                "sparse_mla_attention_page_gb300/csrc/tc_ptx.cuh"]
-ATTN_KERNEL = "sparse_attn_tc_kernel (one launch per attention call)"
+                "sparse_mla_attention_page_gb300/csrc/tc_ptx.cuh",
+                "sparse_mla_attention_page_gb300/csrc/combine.cu"]
+ATTN_KERNEL = "sparse_attn_tc_kernel + combine_kernel (the attention call)"
 COMPUTE_DTYPE = "e4m3"         # tcgen05 kind::f8f6f4 MMAs (E4M3 operands, FP32 accumulation)
 
 
@@ -272,7 +273,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
             binding.dsa_sparse_attn_decode(q, pool, layout, topk, w["sm_scale"], o, lse, ws,
                                            page_table=pt, page_size=w["page_size"])
 
-    launches_per_step = 1 + (1 if prefill else 0) + 1      # writer, [q8 quantiser], attention
+    # writer, [q8 quantiser], attention, [split-unit merge when a unit spans CTAs]
+    launches_per_step = 1 + (1 if prefill else 0) + 1 + (1 if ws is not None else 0)
 
     for _ in range(args.warmup):
         flush_buf.zero_()
