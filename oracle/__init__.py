@@ -45,7 +45,7 @@ def load(path: str):
     L.oracle_e4m3_encode.argtypes = [c.c_float]
     L.oracle_e4m3_encode_bruteforce.restype = c.c_uint8
     L.oracle_e4m3_encode_bruteforce.argtypes = [c.c_float]
-    for fn in (L.oracle_kv_write_raw, L.oracle_kv_write_scaled):
+    for fn in (L.oracle_kv_write_raw, L.oracle_kv_write_scaled, L.oracle_kv_write_rope656):
         fn.restype = c.c_int64
         fn.argtypes = [c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_int64]
     L.oracle_e4m3_encode_array.restype = None
@@ -111,8 +111,16 @@ def e4m3_encode_array(x: np.ndarray, bruteforce: bool = False) -> np.ndarray:
     return out
 
 
+LAYOUT_CODES = {"raw512": 0, "scaled528": 1, "rope656": 2}
+
+
 def row_bytes(layout: str) -> int:
-    return {"raw512": 512, "scaled528": 528}[layout]
+    return {"raw512": 512, "scaled528": 528, "rope656": 656}[layout]
+
+
+def key_width(layout: str) -> int:
+    """Query/key width: the 512 latent dims, plus 64 RoPE dims for 656-byte rows."""
+    return 576 if layout == "rope656" else 512
 
 
 def new_pool(pool_rows: int, layout: str) -> np.ndarray:
@@ -120,12 +128,14 @@ def new_pool(pool_rows: int, layout: str) -> np.ndarray:
 
 
 def kv_write(layout: str, x_bf16: np.ndarray, slots: np.ndarray, pool: np.ndarray) -> int:
-    """Write BF16 rows (uint16 bits [n, 512]) into pool rows ``slots`` (in place)."""
+    """Write BF16 rows (uint16 bits [n, 512], or [n, 576] for 656-byte rows) into
+    pool rows ``slots`` (in place)."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     s = np.ascontiguousarray(slots, dtype=np.int64)
     assert pool.flags.c_contiguous and pool.dtype == np.uint8
-    assert pool.shape[1] == row_bytes(layout) and x.shape[1] == 512 and x.shape[0] == s.shape[0]
-    fn = lib().oracle_kv_write_raw if layout == "raw512" else lib().oracle_kv_write_scaled
+    assert pool.shape[1] == row_bytes(layout) and x.shape[1] == key_width(layout) and x.shape[0] == s.shape[0]
+    fn = {"raw512": lib().oracle_kv_write_raw, "scaled528": lib().oracle_kv_write_scaled,
+          "rope656": lib().oracle_kv_write_rope656}[layout]
     n = fn(_ptr(x), x.shape[0], _ptr(s), _ptr(pool), pool.shape[0])
     if n < 0:
         raise ValueError("slot beyond the pool")
@@ -161,7 +171,8 @@ def sparse_attn(pool: np.ndarray, layout: str, topk: np.ndarray, sm_scale: float
         q = np.ascontiguousarray(q8, dtype=np.uint8)
         qs = np.ascontiguousarray(q_scale, dtype=np.float32)
         kind = 1
-    assert q.shape[0] == T and q.shape[2] == 512
+    assert q.shape[0] == T and q.shape[2] == (key_width(layout) if kind == 0 else 512)
+    assert kind == 0 or layout != "rope656", "FP8 queries are defined over the 512 latent dims only"
     H = q.shape[1]
     pool = np.ascontiguousarray(pool, dtype=np.uint8)
     assert pool.shape[1] == row_bytes(layout)
@@ -183,7 +194,7 @@ def sparse_attn(pool: np.ndarray, layout: str, topk: np.ndarray, sm_scale: float
         n_threads = max(1, len(os.sched_getaffinity(0)))
     err = lib().oracle_sparse_attn(
         kind, _ptr(q), _ptr(qs), T, H,
-        _ptr(pool), pool.shape[0], 0 if layout == "raw512" else 1,
+        _ptr(pool), pool.shape[0], LAYOUT_CODES[layout],
         _ptr(pt), B, max_pages, page_size,
         _ptr(ts), _ptr(topk), K, float(np.float32(sm_scale)),
         _ptr(tok), n, _ptr(O), _ptr(LSE), int(n_threads))
@@ -198,7 +209,7 @@ def gather_dequant(pool: np.ndarray, layout: str, topk: np.ndarray, *,
     topk = np.ascontiguousarray(topk, dtype=np.int32)
     T, K = topk.shape
     pool = np.ascontiguousarray(pool, dtype=np.uint8)
-    assert pool.shape[1] == row_bytes(layout)
+    assert layout in ("raw512", "scaled528") and pool.shape[1] == row_bytes(layout)
     if page_table is not None:
         pt = np.ascontiguousarray(page_table, dtype=np.int32)
         B, max_pages = pt.shape

@@ -18,6 +18,10 @@
  *  - Group-scaled 528-byte row: 512 E4M3 values then four FP32 scales, one per
  *    128-value group ("[DSA] Support group-scaled FP8 NoPE KV reads for CUDA
  *    TileLang", "Motivation").  Scale = amax(group)/448, values = e4m3(x/s).
+ *  - 656-byte RoPE row: the group-scaled 528-byte row followed by the 64-dim
+ *    BF16 RoPE part of the key (little-endian), so the query/key width is
+ *    576 and the values stay the 512 latent dims ("[DSA] Support group-scaled
+ *    FP8 NoPE KV reads for CUDA TileLang", Motivation: the 656-byte layout).
  *  - Sparse attention: per query token and head, softmax over the scaled dot
  *    products with the latent rows named by the token's top-k list; -1
  *    entries are masked (pull 44217, "Modifications": padding with -1); the
@@ -46,6 +50,7 @@
 #define ORACLE_D 512
 #define ORACLE_GROUP 128
 #define ORACLE_GROUPS 4
+#define ORACLE_ROPE 64      /* RoPE dims of the 656-byte row */
 
 /* error bits, same meaning as the library's device flag */
 #define ORACLE_ERR_INDEX_RANGE 1
@@ -179,22 +184,49 @@ static float scaled_group(const float* v, uint8_t* q) {
   return s;
 }
 
-/* Group-scaled writer: row = 512 E4M3 bytes, then 4 little-endian FP32 scales
- * at byte offsets 512 + 4g; group g covers dims [128g, 128g + 128). */
+/* The first 528 bytes of a group-scaled row from 512 BF16 values: 512 E4M3
+ * bytes, then 4 little-endian FP32 scales at byte offsets 512 + 4g; group g
+ * covers dims [128g, 128g + 128). */
+static void scaled_row(const uint16_t* x, uint8_t* row) {
+  float v[ORACLE_GROUP];
+  for (int g = 0; g < ORACLE_GROUPS; ++g) {
+    for (int j = 0; j < ORACLE_GROUP; ++j) v[j] = oracle_bf16_to_float(x[g * ORACLE_GROUP + j]);
+    float sc = scaled_group(v, row + g * ORACLE_GROUP);
+    put_le_f32(row + 512 + 4 * g, sc);
+  }
+}
+
+/* Group-scaled writer: 528-byte rows. */
 int64_t oracle_kv_write_scaled(const uint16_t* x, int64_t n_rows, const int64_t* slots,
                                uint8_t* pool, int64_t pool_rows) {
   int64_t written = 0;
-  float v[ORACLE_GROUP];
   for (int64_t i = 0; i < n_rows; ++i) {
     int64_t s = slots[i];
     if (s < 0) continue;
     if (s >= pool_rows) return -1;
-    uint8_t* row = pool + s * 528;
-    for (int g = 0; g < ORACLE_GROUPS; ++g) {
-      for (int j = 0; j < ORACLE_GROUP; ++j)
-        v[j] = oracle_bf16_to_float(x[i * ORACLE_D + g * ORACLE_GROUP + j]);
-      float sc = scaled_group(v, row + g * ORACLE_GROUP);
-      put_le_f32(row + 512 + 4 * g, sc);
+    scaled_row(x + i * ORACLE_D, pool + s * 528);
+    ++written;
+  }
+  return written;
+}
+
+/* RoPE writer: x is [n_rows, 576] BF16; dims [0, 512) go through the group-
+ * scaled writer, dims [512, 576) are stored as they are (BF16, little-endian)
+ * at byte offsets 528 + 2j. */
+int64_t oracle_kv_write_rope656(const uint16_t* x, int64_t n_rows, const int64_t* slots,
+                                uint8_t* pool, int64_t pool_rows) {
+  int64_t written = 0;
+  const int W = ORACLE_D + ORACLE_ROPE;
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t s = slots[i];
+    if (s < 0) continue;
+    if (s >= pool_rows) return -1;
+    uint8_t* row = pool + s * 656;
+    scaled_row(x + i * W, row);
+    for (int j = 0; j < ORACLE_ROPE; ++j) {
+      uint16_t b = x[i * W + ORACLE_D + j];
+      row[528 + 2 * j] = (uint8_t)(b & 0xFF);
+      row[528 + 2 * j + 1] = (uint8_t)(b >> 8);
     }
     ++written;
   }
@@ -233,7 +265,8 @@ typedef struct {
   int T, H;
   const uint8_t* pool;
   int64_t pool_rows;
-  int layout;            /* 0: raw512, 1: scaled528 */
+  int layout;            /* 0: raw512, 1: scaled528, 2: rope656 */
+  int DK;                /* query/key width: 512, or 576 with the RoPE part */
   const int32_t* page_table; /* [B, max_pages] or NULL: indices are physical rows */
   int B, max_pages, page_size;
   const int32_t* token_seq;  /* [T] or NULL: every token in sequence 0 */
@@ -268,17 +301,21 @@ static int64_t resolve_row(const attn_job* J, int t, int32_t idx, int* err) {
   return row;
 }
 
-/* Dequantised latent row in float64. */
+/* Dequantised key row in float64: the 512 latent dims, then (656-byte rows)
+ * the 64 RoPE dims. */
 static void dequant_row(const attn_job* J, int64_t row, double* k) {
   if (J->layout == 0) {
     const uint8_t* r = J->pool + row * 512;
     for (int d = 0; d < ORACLE_D; ++d) k[d] = oracle_e4m3_decode(r[d]);
   } else {
-    const uint8_t* r = J->pool + row * 528;
+    const uint8_t* r = J->pool + row * (J->layout == 1 ? 528 : 656);
     for (int d = 0; d < ORACLE_D; ++d) {
       double s = (double)le_f32(r + 512 + 4 * (d / ORACLE_GROUP));
       k[d] = oracle_e4m3_decode(r[d]) * s;
     }
+    if (J->layout == 2)
+      for (int j = 0; j < ORACLE_ROPE; ++j)
+        k[ORACLE_D + j] = (double)oracle_bf16_to_float((uint16_t)(r[528 + 2 * j] | (r[528 + 2 * j + 1] << 8)));
   }
 }
 
@@ -289,15 +326,15 @@ static void attend_token(attn_job* J, int li, double* rows, double* q, double* s
   for (int j = 0; j < J->K; ++j) {
     int64_t row = resolve_row(J, t, idx[j], err);
     if (row < 0) continue;
-    dequant_row(J, row, rows + (int64_t)n * ORACLE_D);
+    dequant_row(J, row, rows + (int64_t)n * J->DK);
     ++n;
   }
   for (int h = 0; h < J->H; ++h) {
     double* o = J->O + ((int64_t)li * J->H + h) * ORACLE_D;
-    int64_t qoff = ((int64_t)t * J->H + h) * ORACLE_D;
+    int64_t qoff = ((int64_t)t * J->H + h) * J->DK;
     if (J->q_kind == 0) {
       const uint16_t* qb = (const uint16_t*)J->q + qoff;
-      for (int d = 0; d < ORACLE_D; ++d) q[d] = (double)oracle_bf16_to_float(qb[d]);
+      for (int d = 0; d < J->DK; ++d) q[d] = (double)oracle_bf16_to_float(qb[d]);
     } else {
       const uint8_t* q8 = (const uint8_t*)J->q + qoff;
       double sc = (double)J->q_scale[(int64_t)t * J->H + h];
@@ -310,9 +347,9 @@ static void attend_token(attn_job* J, int li, double* rows, double* q, double* s
     }
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
-      const double* k = rows + (int64_t)j * ORACLE_D;
+      const double* k = rows + (int64_t)j * J->DK;
       double dot = 0.0;
-      for (int d = 0; d < ORACLE_D; ++d) dot += q[d] * k[d];
+      for (int d = 0; d < J->DK; ++d) dot += q[d] * k[d];
       s[j] = J->sm_scale * dot;
       if (s[j] > m) m = s[j];
     }
@@ -322,7 +359,7 @@ static void attend_token(attn_job* J, int li, double* rows, double* q, double* s
     for (int d = 0; d < ORACLE_D; ++d) o[d] = 0.0;
     for (int j = 0; j < n; ++j) {
       double p = exp(s[j] - lse);
-      const double* k = rows + (int64_t)j * ORACLE_D;
+      const double* k = rows + (int64_t)j * J->DK;     /* values: the latent dims */
       for (int d = 0; d < ORACLE_D; ++d) o[d] += p * k[d];
     }
     J->LSE[(int64_t)li * J->H + h] = lse;
@@ -331,8 +368,8 @@ static void attend_token(attn_job* J, int li, double* rows, double* q, double* s
 
 static void* attn_worker(void* arg) {
   attn_job* J = (attn_job*)arg;
-  double* rows = (double*)malloc(sizeof(double) * (size_t)J->K * ORACLE_D);
-  double* q = (double*)malloc(sizeof(double) * ORACLE_D);
+  double* rows = (double*)malloc(sizeof(double) * (size_t)J->K * J->DK);
+  double* q = (double*)malloc(sizeof(double) * J->DK);
   double* s = (double*)malloc(sizeof(double) * (size_t)J->K);
   int err = 0;
   for (;;) {
@@ -370,6 +407,7 @@ int oracle_sparse_attn(int q_kind, const void* q, const float* q_scale, int T, i
   }
   J.q_kind = q_kind; J.q = q; J.q_scale = q_scale; J.T = T; J.H = H;
   J.pool = pool; J.pool_rows = pool_rows; J.layout = layout;
+  J.DK = layout == 2 ? ORACLE_D + ORACLE_ROPE : ORACLE_D;
   J.page_table = page_table; J.B = B; J.max_pages = max_pages; J.page_size = page_size;
   J.token_seq = token_seq; J.topk = topk; J.K = K; J.sm_scale = sm_scale;
   J.tokens = tokens; J.n_tokens = n_tokens; J.O = O; J.LSE = LSE;

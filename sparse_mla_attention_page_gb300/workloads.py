@@ -17,6 +17,9 @@ Workloads (all 512-dim NoPE latent rows, page size 64, sm_scale = 1/sqrt(576)):
 * ``decode_scaled528``     128 tokens, 32 heads, 131072-row pool of
   N(0,1)*U(0.1,4) rows (one multiplier per row), top-k 2048 drawn with
   replacement (duplicates allowed), 5 % of entries -1 at random positions.
+* ``decode_rope656``       64 tokens, 16 heads, 131072-row pool of 656-byte
+  rows (group-scaled latent N(0,1)*U(0.1,4) per row plus a 64-dim BF16 RoPE
+  part N(0,1)), 576-wide queries, top-k 2048 distinct, 5 % -1.
 * ``prefill_q8_raw512``    4096 query tokens at positions 0..4095 after 8192
   context rows of one sequence, 32 heads, 16384-row pool; token at position
   p draws min(2048, 8193 + p) distinct causal indices from [0, 8192 + p],
@@ -39,6 +42,7 @@ import math
 import numpy as np
 
 D_LATENT = 512
+D_ROPE = 64          # RoPE dims of a 656-byte row
 PAGE_SIZE = 64
 SM_SCALE = 1.0 / math.sqrt(576.0)
 
@@ -46,6 +50,7 @@ WORKLOADS = (
     "tiny_decode_raw512",
     "decode_raw512",
     "decode_scaled528",
+    "decode_rope656",
     "prefill_q8_raw512",
     "prefill_q8_scaled528",
     "writer_sweep",
@@ -138,6 +143,26 @@ def decode_scaled528(seed: int = 3, T: int = 128, H: int = 32, K: int = 2048,
                 token_seq=None, topk=topk, sm_scale=SM_SCALE)
 
 
+def decode_rope656(seed: int = 7, T: int = 64, H: int = 16, K: int = 2048,
+                   pool_rows: int = 131072, masked_frac: float = 0.05) -> dict:
+    """Decode over 656-byte rows: the group-scaled latent (N(0,1) * U(0.1, 4) per
+    row) plus a 64-dim BF16 RoPE part N(0,1); queries are 576 wide."""
+    rng = rng_for(seed)
+    q = f32_to_bf16_bits(rng.standard_normal((T, H, D_LATENT + D_ROPE), dtype=np.float32))
+    mult = rng.uniform(0.1, 4.0, size=(pool_rows, 1)).astype(np.float32)
+    nope = rng.standard_normal((pool_rows, D_LATENT), dtype=np.float32) * mult
+    rope = rng.standard_normal((pool_rows, D_ROPE), dtype=np.float32)
+    kv_src = f32_to_bf16_bits(np.concatenate([nope, rope], axis=1))
+    pages = pool_rows // PAGE_SIZE
+    page_table = _shuffled_page_table(rng, pages, pages)
+    topk = _distinct_indices(rng, T, K, pool_rows)
+    topk[rng.random((T, K)) < masked_frac] = -1
+    return dict(name="decode_rope656", layout="rope656", T=T, H=H, K=K,
+                q_bf16=q, kv_src=kv_src, kv_slots=np.arange(pool_rows, dtype=np.int64),
+                pool_rows=pool_rows, page_table=page_table, page_size=PAGE_SIZE,
+                token_seq=None, topk=topk, sm_scale=SM_SCALE)
+
+
 def prefill_q8_raw512(seed: int = 4, T: int = 4096, H: int = 32, K: int = 2048,
                       context: int = 8192, pool_rows: int = 16384,
                   first_pos: int = 0) -> dict:
@@ -207,6 +232,7 @@ def make(name: str, **kw) -> dict:
         "tiny_decode_raw512": tiny_decode_raw512,
         "decode_raw512": decode_raw512,
         "decode_scaled528": decode_scaled528,
+        "decode_rope656": decode_rope656,
         "prefill_q8_raw512": prefill_q8_raw512,
         "prefill_q8_scaled528": prefill_q8_scaled528,
         "writer_sweep": writer_sweep,

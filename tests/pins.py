@@ -423,10 +423,39 @@ def pin_gather_dequant_torch():
     assert err2 == oracle.ERR_INDEX_RANGE and idx2[0, 0] == -1
 
 
+def pin_rope656():
+    """656-byte rows: the latent part is byte-identical to the group-scaled
+    writer's row, the RoPE part is the input BF16 bits; attention over 576-wide
+    keys with 512-wide values equals PyTorch's float64 scaled_dot_product_attention
+    and logsumexp."""
+    w = W.decode_rope656(seed=91, T=4, H=3, K=256, pool_rows=2048)
+    pool = oracle.fill_pool(w)
+    ref = oracle.new_pool(w["pool_rows"], "scaled528")
+    oracle.kv_write("scaled528", np.ascontiguousarray(w["kv_src"][:, :512]), w["kv_slots"], ref)
+    np.testing.assert_array_equal(pool[:, :528], ref)
+    np.testing.assert_array_equal(pool[:, 528:].view("<u2"), w["kv_src"][:, 512:])
+    O, L, err = oracle.sparse_attn(pool, "rope656", w["topk"], w["sm_scale"], q_bf16=w["q_bf16"],
+                                   page_table=w["page_table"], page_size=64, n_threads=2)
+    assert err == 0
+    q = torch.from_numpy(w["q_bf16"].astype(np.int16)).view(torch.bfloat16).to(torch.float64)
+    for t in range(w["T"]):
+        idx = w["topk"][t]
+        idx = idx[idx >= 0]
+        rows = np.array([_phys(w["page_table"], None, t, int(i)) for i in idx])
+        nope = torch.from_numpy(_pool_rows_f64(pool[:, :528], "scaled528", rows))
+        rope = torch.from_numpy(np.ascontiguousarray(pool[rows, 528:]).view(np.int16)).view(torch.bfloat16)
+        k = torch.cat([nope, rope.to(torch.float64)], dim=1)             # [n, 576]
+        sc = float(np.float32(w["sm_scale"]))
+        o = torch.nn.functional.scaled_dot_product_attention(q[t][:, None, :], k[None].expand(w["H"], -1, -1),
+                                                             nope[None].expand(w["H"], -1, -1), scale=sc)
+        np.testing.assert_allclose(O[t], o[:, 0].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(L[t], torch.logsumexp((q[t] @ k.T) * sc, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [
     pin_decode_spec, pin_decode_torch, pin_encode_exhaustive_bf16, pin_encode_ties_and_f32,
     pin_encode_roundtrip, pin_scaled_worked_example, pin_raw_writer_torch,
     pin_scaled_writer_invariants, pin_attn_sdpa, pin_attn_closed_forms, pin_attn_invariances,
     pin_q8_matches_bf16_decode, pin_q8_quantiser, pin_error_bits, pin_wrong_index_is_detected,
-    pin_gather_dequant_torch,
+    pin_gather_dequant_torch, pin_rope656,
 ]

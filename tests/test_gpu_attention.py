@@ -183,6 +183,18 @@ def test_topk_widths(K):
     assert_attn_close(O, L, Or, Lr, f"K={K}")
 
 
+@pytest.mark.parametrize("T,K,layout", [(1, 8192, "raw512"), (2, 16384, "raw512"), (1, 4096, "scaled528")])
+def test_unit_spread_over_many_ctas(T, K, layout):
+    """Few tokens with long top-k lists: each (token, head group) is split over
+    dozens of CTAs, so the merge folds many partial results (several batches)."""
+    w = _small(T=T, K=K, pool_rows=32768, layout=layout)
+    pool, pd = pool_for(w, ("spread", T, K, layout))
+    O, L, err = run_decode(w, pd)
+    Or, Lr, _ = oracle_decode(w, pool)
+    assert err == 0
+    assert_attn_close(O, L, Or, Lr, f"T={T} K={K} {layout}")
+
+
 def test_multi_sequence_page_tables():
     """Tokens of three sequences, each with its own page table row."""
     rng = np.random.default_rng(201)

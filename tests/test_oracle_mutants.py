@@ -24,7 +24,7 @@ MUTANTS = {
                           "uint8_t sign = (x < 0) ? 0x80 : 0x00;\n  if (isnan(x)) return (uint8_t)(sign | 0x7F);\n  double a = fabs((double)x);\n  if (a >= 448.0) return (uint8_t)(sign | 0x7E);\n  int lo"),
     "scale_divisor": ("  float s = amax / 448.0f;\n  for (int i = 0; i < ORACLE_GROUP; ++i) {",
                       "  float s = amax / 447.0f;\n  for (int i = 0; i < ORACLE_GROUP; ++i) {"),
-    "writer_group_stride": ("x[i * ORACLE_D + g * ORACLE_GROUP + j]", "x[i * ORACLE_D + g * 64 + j]"),
+    "writer_group_stride": ("oracle_bf16_to_float(x[g * ORACLE_GROUP + j]);", "oracle_bf16_to_float(x[g * 64 + j]);"),
     "scale_word_order": ("put_le_f32(row + 512 + 4 * g, sc);", "put_le_f32(row + 524 - 4 * g, sc);"),
     "scale_endianness": ("p[0] = (uint8_t)(u & 0xFF);", "p[3] = (uint8_t)(u & 0xFF);"),
     "read_group_mapping": ("le_f32(r + 512 + 4 * (d / ORACLE_GROUP))", "le_f32(r + 512 + 4 * (d % 4))"),
@@ -42,6 +42,11 @@ MUTANTS = {
                               "if (page >= J->max_pages) { return -1; }"),
     "reader_bf16_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;"),
     "reader_scale_group": ("const int g = d / ORACLE_GROUP;", "const int g = d % 4;"),
+    "rope_ignored_in_keys": ("k[ORACLE_D + j] = (double)oracle_bf16_to_float((uint16_t)(r[528 + 2 * j] | (r[528 + 2 * j + 1] << 8)));",
+                             "k[ORACLE_D + j] = 0.0;"),
+    "rope_read_byte_order": ("(uint16_t)(r[528 + 2 * j] | (r[528 + 2 * j + 1] << 8))",
+                             "(uint16_t)(r[528 + 2 * j + 1] | (r[528 + 2 * j] << 8))"),
+    "rope_write_byte_order": ("row[528 + 2 * j] = (uint8_t)(b & 0xFF);", "row[528 + 2 * j] = (uint8_t)(b >> 8);"),
     "reader_index_not_remapped": ("idx_out[e] = row < 0 ? -1 : (int32_t)e;", "idx_out[e] = row < 0 ? -1 : topk[e];"),
 }
 
