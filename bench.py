@@ -46,6 +46,11 @@ ATTN_KERNEL = "sparse_attn_tc_kernel + combine_kernel (the attention call)"
 COMPUTE_DTYPE = "e4m3"         # tcgen05 kind::f8f6f4 MMAs (E4M3 operands, FP32 accumulation)
 
 
+ROW_BYTES = {"raw512": 512, "scaled528": 528, "rope656": 656}
+WRITERS = {"raw512": lambda b: b.dsa_kv_write_raw, "scaled528": lambda b: b.dsa_kv_write_scaled,
+           "rope656": lambda b: b.dsa_kv_write_rope656}
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -73,7 +78,8 @@ def step_rows(w: dict) -> tuple[np.ndarray, np.ndarray]:
     """The batch's new latent rows (one per query token) and their slots: the
     last T physical rows of the pool (re-written with the same bytes each step)."""
     rng = W.rng_for(9000 + w["T"])
-    x = W.f32_to_bf16_bits(rng.standard_normal((w["T"], 512), dtype=np.float32))
+    width = 576 if w["layout"] == "rope656" else 512
+    x = W.f32_to_bf16_bits(rng.standard_normal((w["T"], width), dtype=np.float32))
     slots = np.arange(w["pool_rows"] - w["T"], w["pool_rows"], dtype=np.int64)
     return x, slots
 
@@ -82,15 +88,18 @@ def algorithmic_bytes(w: dict) -> int:
     """Bytes the attention call must move: each valid entry's row once, plus the
     query, q_scale, top-k list, O and LSE."""
     T, H, K = w["T"], w["H"], w["K"]
-    R = 512 if w["layout"] == "raw512" else 528
+    R = ROW_BYTES[w["layout"]]
     valid = W.valid_entry_count(w["topk"])
     q8 = w["name"].startswith("prefill_q8")
-    q_bytes = T * H * 512 * (1 if q8 else 2) + (T * H * 4 if q8 else 0)
+    q_width = 576 if w["layout"] == "rope656" else 512
+    q_bytes = T * H * q_width * (1 if q8 else 2) + (T * H * 4 if q8 else 0)
     return valid * R + q_bytes + T * K * 4 + T * H * 512 * 2 + T * H * 4
 
 
 def attn_flops(w: dict) -> int:
-    return 4 * w["H"] * 512 * W.valid_entry_count(w["topk"])
+    """QK^T over the key width (576 with RoPE) and PV over the 512 latent dims."""
+    dk = 576 if w["layout"] == "rope656" else 512
+    return 2 * w["H"] * (dk + 512) * W.valid_entry_count(w["topk"])
 
 
 def run_gather(args) -> dict:
@@ -241,8 +250,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     def bf16(a):
         return to_dev(a.view(np.int16), torch.bfloat16)
 
-    write = binding.dsa_kv_write_raw if layout == "raw512" else binding.dsa_kv_write_scaled
-    pool = torch.zeros(w["pool_rows"], 512 if layout == "raw512" else 528, dtype=torch.uint8, device=dev)
+    write = WRITERS[layout](binding)
+    pool = torch.zeros(w["pool_rows"], ROW_BYTES[layout], dtype=torch.uint8, device=dev)
     kv_src = bf16(w["kv_src"])
     write(kv_src, to_dev(w["kv_slots"]), pool)
     del kv_src

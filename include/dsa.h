@@ -48,8 +48,13 @@ extern "C" {
  *  DSA_KV_RAW512     512 unscaled E4M3 bytes per row.
  *  DSA_KV_SCALED528  512 E4M3 bytes, then four little-endian FP32 scales at
  *                    byte offsets 512 + 4g; scale g applies to dims
- *                    [128g, 128g + 128): value = e4m3(byte) * scale_g. */
-typedef enum { DSA_KV_RAW512 = 0, DSA_KV_SCALED528 = 1 } dsa_kv_layout;
+ *                    [128g, 128g + 128): value = e4m3(byte) * scale_g.
+ *  DSA_KV_ROPE656    the 528-byte row, then the 64 RoPE dims of the key as
+ *                    little-endian BF16 at byte offsets 528 + 2j: keys and
+ *                    queries are 576 wide, values are the 512 latent dims
+ *                    ["[DSA] Support group-scaled FP8 NoPE KV reads for CUDA
+ *                    TileLang", Motivation: the 656-byte layout]. */
+typedef enum { DSA_KV_RAW512 = 0, DSA_KV_SCALED528 = 1, DSA_KV_ROPE656 = 2 } dsa_kv_layout;
 
 enum {
   DSA_OK = 0,
@@ -106,6 +111,14 @@ int dsa_kv_write_raw(const void* x_bf16_dev, int64_t n_rows, const int64_t* slot
 int dsa_kv_write_scaled(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
                         void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream);
 
+/* Same for the 656-byte RoPE layout: x_bf16_dev is [n_rows, 576]; dims
+ * [0, 512) are written as by dsa_kv_write_scaled, dims [512, 576) are stored
+ * unchanged (BF16) at byte offsets 528 + 2j.
+ *   x_bf16_dev  [n_rows, 576] BF16, 16-byte aligned.
+ *   pool_dev    [pool_rows, 656] bytes, 16-byte aligned. */
+int dsa_kv_write_rope656(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
+                         void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream);
+
 /* FP8 query quantiser (NoPE query preparation with a zero-dim RoPE part,
  * [P3 Modifications: zero-dimensional RoPE queries]): per vector of 512 dims
  * (one token and head), scale = amax / 448 (FP32), q8 = e4m3_satrne(q / scale);
@@ -140,7 +153,10 @@ size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
  * LSE = -inf.  Duplicate indices count once per slot.
  *
  *   q_bf16_dev      [T, H, 512] BF16, 16-byte aligned.
- *   D, kv_row_dim   must both be 512 (else DSA_ERR_ROW_WIDTH).
+ *   D, kv_row_dim   must both be 512, or both 576 with DSA_KV_ROPE656 (else
+ *                   DSA_ERR_ROW_WIDTH); over 656-byte rows the query is
+ *                   [T, H, 576] (latent dims, then the 64 RoPE dims), the
+ *                   scores use all 576 dims and O the 512 latent dims.
  *   pool_dev        [pool_rows, 512 or 528] bytes, 16-byte aligned.
  *   page_table_dev  [B, max_pages] int32 physical page ids, or NULL.
  *   token_seq_dev   [T] int32 sequence id per token, or NULL (all sequence 0).
@@ -149,7 +165,8 @@ size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
  *   lse_dev         [T, H] float out.
  *   workspace_dev   ws_bytes >= dsa_sparse_attn_workspace_bytes(T, H, K).
  *   err_flag_dev    nullable int32 error bits.
- * H must be one of 8, 16, 32, 64, 128.  T == 0 is a no-op. */
+ * H must be one of 8, 16, 32, 64, 128 (8 or 16 over 656-byte rows).
+ * T == 0 is a no-op. */
 int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D,
                            const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
                            const int32_t* page_table_dev, int B, int max_pages, int page_size,

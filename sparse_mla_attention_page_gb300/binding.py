@@ -19,7 +19,8 @@ from . import build as _build
 
 DSA_KV_RAW512 = 0
 DSA_KV_SCALED528 = 1
-LAYOUTS = {"raw512": DSA_KV_RAW512, "scaled528": DSA_KV_SCALED528}
+DSA_KV_ROPE656 = 2
+LAYOUTS = {"raw512": DSA_KV_RAW512, "scaled528": DSA_KV_SCALED528, "rope656": DSA_KV_ROPE656}
 
 DSA_DEV_ERR_INDEX_RANGE = 1
 DSA_DEV_ERR_PAGE_RANGE = 2
@@ -31,7 +32,7 @@ _lib = None
 
 # Every symbol include/dsa.h declares.
 EXPORTS = (
-    "dsa_status_string", "dsa_kv_row_bytes", "dsa_kv_write_raw", "dsa_kv_write_scaled",
+    "dsa_status_string", "dsa_kv_row_bytes", "dsa_kv_write_raw", "dsa_kv_write_scaled", "dsa_kv_write_rope656",
     "dsa_quantize_q8", "dsa_sparse_attn_workspace_bytes", "dsa_sparse_attn_decode",
     "dsa_sparse_attn_prefill_q8", "dsa_gather_dequant", "dsa_sparse_attn_decode_noalloc",
 )
@@ -63,7 +64,7 @@ def lib() -> ctypes.CDLL:
             L.dsa_status_string.argtypes = [i32]
             L.dsa_kv_row_bytes.restype = c.c_size_t
             L.dsa_kv_row_bytes.argtypes = [i32]
-            for f in (L.dsa_kv_write_raw, L.dsa_kv_write_scaled):
+            for f in (L.dsa_kv_write_raw, L.dsa_kv_write_scaled, L.dsa_kv_write_rope656):
                 f.restype = i32
                 f.argtypes = [vp, i64, vp, vp, i64, vp, vp]
             L.dsa_quantize_q8.restype = i32
@@ -120,13 +121,13 @@ def dsa_kv_row_bytes(layout) -> int:
     return int(lib().dsa_kv_row_bytes(LAYOUTS.get(layout, layout)))
 
 
-def _write(fn_name, x_bf16, slots, pool, err_flag, stream):
-    _need(x_bf16, "x_bf16", torch.bfloat16, 512)
+def _write(fn_name, x_bf16, slots, pool, err_flag, stream, width=512):
+    _need(x_bf16, "x_bf16", torch.bfloat16, width)
     _need(slots, "slots", torch.int64)
     _need(pool, "pool", torch.uint8)
     if err_flag is not None:
         _need(err_flag, "err_flag", torch.int32)
-    n = x_bf16.numel() // 512
+    n = x_bf16.numel() // width
     if slots.numel() != n:
         raise ValueError("slots must have one entry per row")
     rows = pool.shape[0]
@@ -146,6 +147,14 @@ def dsa_kv_write_scaled(x_bf16, slots, pool, err_flag=None, stream=None) -> None
     if pool.dim() != 2 or pool.shape[1] != 528:
         raise ValueError("scaled pool must be [rows, 528] uint8")
     _write("dsa_kv_write_scaled", x_bf16, slots, pool, err_flag, stream)
+
+
+def dsa_kv_write_rope656(x_bf16, slots, pool, err_flag=None, stream=None) -> None:
+    """pool [rows, 656] uint8 <- group-scaled e4m3(x[:, :512]) and the BF16 RoPE
+    dims x[:, 512:576] at rows ``slots``."""
+    if pool.dim() != 2 or pool.shape[1] != 656:
+        raise ValueError("RoPE pool must be [rows, 656] uint8")
+    _write("dsa_kv_write_rope656", x_bf16, slots, pool, err_flag, stream, width=576)
 
 
 def dsa_quantize_q8(q_bf16, q8, q_scale, stream=None) -> None:
@@ -225,15 +234,19 @@ def dsa_gather_dequant(pool, layout, topk, out, idx_out, page_table=None, page_s
 
 
 def _kv_row_dim(pool, lay) -> int:
-    """Latent width held by one pool row (528-byte rows carry 16 bytes of scales)."""
+    """Key width held by one pool row (528- and 656-byte rows carry 16 bytes of
+    scales; 656-byte rows add 64 BF16 RoPE dims)."""
+    if lay == DSA_KV_ROPE656:
+        return 512 + (pool.shape[1] - 528) // 2
     return pool.shape[1] - (16 if lay == DSA_KV_SCALED528 else 0)
 
 
 def dsa_sparse_attn_decode(q_bf16, pool, layout, topk, sm_scale, o, lse, workspace=None,
                            page_table=None, page_size=64, token_seq=None, err_flag=None,
                            stream=None) -> None:
-    """Sparse MLA decode with BF16 queries [T, H, 512] (see include/dsa.h)."""
-    _need(q_bf16, "q_bf16", torch.bfloat16, 512)
+    """Sparse MLA decode with BF16 queries [T, H, 512] ([T, H, 576] over 656-byte
+    rows; see include/dsa.h)."""
+    _need(q_bf16, "q_bf16", torch.bfloat16, 576 if LAYOUTS.get(layout, layout) == DSA_KV_ROPE656 else 512)
     T, H, lay, B, max_pages, ws_bytes = _attn_common(q_bf16, pool, layout, topk, o, lse,
                                                      page_table, token_seq, workspace, err_flag)
     st = lib().dsa_sparse_attn_decode(
@@ -266,7 +279,7 @@ def dsa_sparse_attn_decode_noalloc(q_bf16, pool, layout, topk, sm_scale, o, lse,
                                    page_size=64, token_seq=None, err_flag=None, stream=None) -> None:
     """Decode using the library's own static workspace (no allocation by anyone);
     see include/dsa.h for its size limit and the sharing rules."""
-    _need(q_bf16, "q_bf16", torch.bfloat16, 512)
+    _need(q_bf16, "q_bf16", torch.bfloat16, 576 if LAYOUTS.get(layout, layout) == DSA_KV_ROPE656 else 512)
     T, H, lay, B, max_pages, _ = _attn_common(q_bf16, pool, layout, topk, o, lse,
                                               page_table, token_seq, None, err_flag)
     st = lib().dsa_sparse_attn_decode_noalloc(

@@ -54,14 +54,14 @@ int validate_writer(const void* x, int64_t n_rows, const int64_t* slots, const v
   return DSA_OK;
 }
 
-int write_rows(bool scaled, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
+int write_rows(int layout, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
                int64_t pool_rows, int32_t* err, void* stream) {
-  int st = validate_writer(x, n_rows, slots, pool, pool_rows, scaled ? 528 : 512);
+  int st = validate_writer(x, n_rows, slots, pool, pool_rows, (int64_t)dsa_kv_row_bytes(layout));
   if (st != DSA_OK || n_rows == 0) return st;
   int sms = 0;
   if ((st = current_device_sms(&sms)) != DSA_OK) return st;
   cudaGetLastError();  // a stale error from earlier work is not this call's
-  dsa::launch_kv_write(scaled, x, n_rows, slots, pool, pool_rows, err, sms,
+  dsa::launch_kv_write(layout, x, n_rows, slots, pool, pool_rows, err, sms,
                        static_cast<cudaStream_t>(stream));
   return launch_status();
 }
@@ -72,10 +72,12 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
                 float sm_scale, void* o, float* lse, void* ws, size_t ws_bytes, int32_t* err,
                 void* stream) {
   if (T < 0 || pool_rows < 0) return DSA_ERR_SHAPE;
-  if (D != 512 || kv_row_dim != 512) return DSA_ERR_ROW_WIDTH;
-  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528) return DSA_ERR_LAYOUT;
+  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528 && layout != DSA_KV_ROPE656) return DSA_ERR_LAYOUT;
+  const int width = layout == DSA_KV_ROPE656 ? 576 : 512;
+  if (D != width || kv_row_dim != width) return DSA_ERR_ROW_WIDTH;
+  if (q8 && layout == DSA_KV_ROPE656) return DSA_ERR_LAYOUT;
   if (K <= 0 || K % 128 != 0) return DSA_ERR_TOPK_PAD;
-  if (!heads_ok(H)) return DSA_ERR_HEADS;
+  if (!heads_ok(H) || (layout == DSA_KV_ROPE656 && H > 16)) return DSA_ERR_HEADS;
   if (T == 0) return DSA_OK;
   if (q == nullptr || pool == nullptr || topk == nullptr || o == nullptr || lse == nullptr ||
       (q8 && q_scale == nullptr))
@@ -101,9 +103,11 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   a.q_scale = q_scale;
   a.T = T;
   a.H = H;
+  a.q_row = layout == DSA_KV_ROPE656 ? 576 : 512;
   a.pool = static_cast<const uint8_t*>(pool);
   a.pool_rows = pool_rows;
-  a.scaled = layout == DSA_KV_SCALED528;
+  a.scaled = layout == DSA_KV_SCALED528 || layout == DSA_KV_ROPE656;
+  a.rope = layout == DSA_KV_ROPE656;
   a.page_table = page_table;
   a.B = B;
   a.max_pages = max_pages;
@@ -152,17 +156,23 @@ const char* dsa_status_string(int status) {
 size_t dsa_kv_row_bytes(int layout) {
   if (layout == DSA_KV_RAW512) return 512;
   if (layout == DSA_KV_SCALED528) return 528;
+  if (layout == DSA_KV_ROPE656) return 656;
   return 0;
 }
 
 int dsa_kv_write_raw(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
                      void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream) {
-  return write_rows(false, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
+  return write_rows(DSA_KV_RAW512, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
 }
 
 int dsa_kv_write_scaled(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
                         void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream) {
-  return write_rows(true, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
+  return write_rows(DSA_KV_SCALED528, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
+}
+
+int dsa_kv_write_rope656(const void* x_bf16_dev, int64_t n_rows, const int64_t* slots_dev,
+                         void* pool_dev, int64_t pool_rows, int32_t* err_flag_dev, void* stream) {
+  return write_rows(DSA_KV_ROPE656, x_bf16_dev, n_rows, slots_dev, pool_dev, pool_rows, err_flag_dev, stream);
 }
 
 int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* q_scale_dev,

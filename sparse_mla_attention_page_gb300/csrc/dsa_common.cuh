@@ -12,6 +12,8 @@ constexpr int kD = 512;          // latent width (kv_lora_rank, RoPE dim 0)
 constexpr int kGroup = 128;      // dims per FP32 scale in the 528-byte row
 constexpr int kRawRow = 512;
 constexpr int kScaledRow = 528;
+constexpr int kRopeRow = 656;    // 528-byte row + 64 BF16 RoPE dims
+constexpr int kRopeDims = 64;
 
 __device__ __forceinline__ void set_err(int32_t* flag, int bits) {
   if (flag != nullptr) atomicOr(flag, bits);

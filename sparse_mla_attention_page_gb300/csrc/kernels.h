@@ -5,7 +5,7 @@
 
 namespace dsa {
 
-void launch_kv_write(bool scaled, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
+void launch_kv_write(int layout, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
                      int64_t pool_rows, int32_t* err, int sms, cudaStream_t stream);
 
 void launch_quantize_q8(const void* q, int64_t n_vec, void* q8, float* scale, int sms,
@@ -22,9 +22,11 @@ struct AttnArgs {
   const void* q;          // BF16 [T,H,512] or E4M3 [T,H,512]
   const float* q_scale;   // [T,H] for FP8 queries, else nullptr
   int T, H;
+  int q_row;              // elements per query row: 512, or 576 over 656-byte rows
   const uint8_t* pool;
   int64_t pool_rows;
-  bool scaled;            // 528-byte rows
+  bool scaled;            // 528-byte (or 656-byte) rows: group scales
+  bool rope;              // 656-byte rows: 64 BF16 RoPE dims after the scales
   const int32_t* page_table;
   int B, max_pages, page_size;
   const int32_t* token_seq;
@@ -59,7 +61,8 @@ void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
 struct GatherArgs {
   const uint8_t* pool;
   int64_t pool_rows;
-  bool scaled;            // 528-byte rows
+  bool scaled;            // 528-byte (or 656-byte) rows: group scales
+  bool rope;              // 656-byte rows: 64 BF16 RoPE dims after the scales
   const int32_t* page_table;
   int B, max_pages, page_size;
   const int32_t* token_seq;

@@ -56,9 +56,14 @@ __global__ void __launch_bounds__(256) kv_write_raw_kernel(
 
 // Group g of 128 dims is held by 16 lanes: groups 0 and 2 by lanes 0-15
 // (first and second half of their registers), groups 1 and 3 by lanes 16-31.
+// kRope: 656-byte rows, whose input rows are 576 wide; the 64 RoPE dims are
+// stored as they are (BF16) after the scales, one 4-byte pair per lane.
+template <bool kRope>
 __global__ void __launch_bounds__(256) kv_write_scaled_kernel(
     const uint16_t* __restrict__ x, int64_t n_rows, const int64_t* __restrict__ slots,
     uint8_t* __restrict__ pool, int64_t pool_rows, int32_t* err) {
+  constexpr int kIn = kRope ? kD + kRopeDims : kD;
+  constexpr int kRowBytes = kRope ? kRopeRow : kScaledRow;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n_rows; i += nwarps) {
@@ -69,7 +74,9 @@ __global__ void __launch_bounds__(256) kv_write_scaled_kernel(
       continue;
     }
     Row16 r;
-    load_row16(x + i * kD, lane, r);
+    load_row16(x + i * kIn, lane, r);
+    uint32_t rope_pair = 0;
+    if (kRope) rope_pair = __ldg(reinterpret_cast<const uint32_t*>(x + i * kIn + kD) + lane);
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -88,8 +95,9 @@ __global__ void __launch_bounds__(256) kv_write_scaled_kernel(
       r.v[k] = s0 == 0.f ? 0.f : __fdiv_rn(r.v[k], s0);
       r.v[8 + k] = s1 == 0.f ? 0.f : __fdiv_rn(r.v[8 + k], s1);
     }
-    uint8_t* row = pool + s * kScaledRow;
+    uint8_t* row = pool + s * kRowBytes;
     store_row16(row, lane, r);
+    if (kRope) reinterpret_cast<uint32_t*>(row + kScaledRow)[lane] = rope_pair;
     const float g1 = __shfl_sync(0xffffffffu, s0, 16);
     const float g3 = __shfl_sync(0xffffffffu, s1, 16);
     if (lane == 0) {
@@ -128,12 +136,15 @@ int writer_grid(int64_t n_rows, int sms) {
 
 }  // namespace
 
-void launch_kv_write(bool scaled, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
+void launch_kv_write(int layout, const void* x, int64_t n_rows, const int64_t* slots, void* pool,
                      int64_t pool_rows, int32_t* err, int sms, cudaStream_t stream) {
   const int grid = writer_grid(n_rows, sms);
-  if (scaled)
-    kv_write_scaled_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), n_rows, slots,
-                                                     static_cast<uint8_t*>(pool), pool_rows, err);
+  if (layout == DSA_KV_ROPE656)
+    kv_write_scaled_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), n_rows, slots,
+                                                           static_cast<uint8_t*>(pool), pool_rows, err);
+  else if (layout == DSA_KV_SCALED528)
+    kv_write_scaled_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), n_rows, slots,
+                                                            static_cast<uint8_t*>(pool), pool_rows, err);
   else
     kv_write_raw_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), n_rows, slots,
                                                   static_cast<uint8_t*>(pool), pool_rows, err);

@@ -63,10 +63,11 @@ extern "C" int dsa_sparse_attn_decode_noalloc(const void* q_bf16_dev, int T, int
                                               float* lse_dev, int32_t* err_flag_dev, void* stream) {
   // the same first checks, in the same order, as dsa_sparse_attn_decode
   if (T < 0 || pool_rows < 0) return DSA_ERR_SHAPE;
-  if (D != 512 || kv_row_dim != 512) return DSA_ERR_ROW_WIDTH;
-  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528) return DSA_ERR_LAYOUT;
+  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528 && layout != DSA_KV_ROPE656) return DSA_ERR_LAYOUT;
+  const int width = layout == DSA_KV_ROPE656 ? 576 : 512;
+  if (D != width || kv_row_dim != width) return DSA_ERR_ROW_WIDTH;
   if (K <= 0 || K % 128 != 0) return DSA_ERR_TOPK_PAD;
-  if (!heads_supported(H)) return DSA_ERR_HEADS;
+  if (!heads_supported(H) || (layout == DSA_KV_ROPE656 && H > 16)) return DSA_ERR_HEADS;
   if (T == 0) return DSA_OK;
   if (dsa_sparse_attn_workspace_bytes(T, H, K) > kScratchBytes) return DSA_ERR_WORKSPACE;
   void* ws = nullptr;

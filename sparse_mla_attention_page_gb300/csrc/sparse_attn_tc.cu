@@ -108,16 +108,19 @@ struct Misc {
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
 static_assert(offsetof(Misc, ring) % 16 == 0 && offsetof(Misc, qsig) % 16 == 0, "vector access alignment");
 
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 struct Cfg {
   static constexpr int HPT = HG / 2;                           // heads per softmax thread
   static constexpr int G = kScaled ? 4 : 1;                    // score accumulators per tile
   static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : 2 * HG;  // QK^T N (query operand rows)
   static constexpr int NP = (3 * HG + 15) / 16 * 16;          // PV N: P hi, mid, lo rows (+ zero pad)
   static constexpr int O_COLS = 4 * NP;
-  static constexpr int GC = (G * NQ + O_COLS <= 512) ? G : G / 2;   // groups per QK^T chunk
+  // 656-byte rows: the RoPE part of the scores, S_rope = K_rope Q_rope^T (BF16
+  // MMAs, N = NR query rows), accumulated in NR more columns of each score buffer
+  static constexpr int NR = kRope ? (HG < 16 ? 16 : HG) : 0;
+  static constexpr int GC = (G * NQ + NR + O_COLS <= 512) ? G : G / 2;   // groups per QK^T chunk
   static constexpr int NQC = G / GC;                          // QK^T chunks per tile
-  static constexpr int S_COLS = GC * NQ;
+  static constexpr int S_COLS = GC * NQ + NR;
   static constexpr int NS = (2 * S_COLS + O_COLS <= 512) ? 2 : 1;
   static constexpr int O_COL0 = NS * S_COLS;
   static constexpr int USED = O_COL0 + O_COLS;
@@ -125,22 +128,29 @@ struct Cfg {
       USED <= 32 ? 32 : USED <= 64 ? 64 : USED <= 128 ? 128 : USED <= 256 ? 256 : 512;
   static constexpr int Q_BYTES = NQ * 512;
   static constexpr int P_BYTES = G * NP * 128;
-  static constexpr int STAGE = kStage + (kScaled ? kScStage : 0);
+  static constexpr int ROPE_STAGE = kRope ? kRows * 128 : 0;   // RoPE parts of a tile: 128 rows x 128 B
+  static constexpr int QR_BYTES = NR * 128;                    // RoPE query operand
+  static constexpr int STAGE = kStage + (kScaled ? kScStage : 0) + ROPE_STAGE;
   static constexpr int FIXED = kMiscBytes + 1024;             // + alignment slack
   // shared memory: two P buffers first, then a third KV stage, then a second query buffer
   static constexpr int NPB = (2 * STAGE + Q_BYTES + 2 * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
   static constexpr int NST = (3 * STAGE + Q_BYTES + NPB * P_BYTES + FIXED <= kSmemLimit) ? 3 : 2;
-  static constexpr int NQB = (NST * STAGE + 2 * Q_BYTES + NPB * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
+  static constexpr int NQB =
+      (NST * STAGE + 2 * (Q_BYTES + QR_BYTES) + NPB * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
   static constexpr int KV_OFF = 0;
   static constexpr int Q_OFF = KV_OFF + NST * kStage;
-  static constexpr int P_OFF = Q_OFF + NQB * Q_BYTES;
-  static constexpr int SC_OFF = P_OFF + NPB * P_BYTES;
+  static constexpr int QR_OFF = Q_OFF + NQB * Q_BYTES;
+  static constexpr int P_OFF = QR_OFF + NQB * QR_BYTES;
+  static constexpr int ROPE_OFF = P_OFF + NPB * P_BYTES;
+  static constexpr int SC_OFF = ROPE_OFF + NST * ROPE_STAGE;
   static constexpr int MISC_OFF = SC_OFF + (kScaled ? NST * kScStage : 0);
   static constexpr int SMEM = MISC_OFF + kMiscBytes + 1024;
   static_assert(HPT >= 4 && HPT <= 16, "heads per softmax thread");
   static_assert(USED <= 512, "tensor memory budget");
   static_assert(SMEM <= kSmemLimit, "shared memory budget");
   static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && (NP * 128) % 1024 == 0, "operand alignment");
+  static_assert(QR_OFF % 1024 == 0 && ROPE_OFF % 1024 == 0 && QR_BYTES % 1024 == 0, "RoPE operand alignment");
+  static_assert(!kRope || (kScaled && !kQ8 && HG <= 16), "656-byte rows: BF16 queries, at most 16 heads");
 };
 
 // Byte offset of element (n, k) in a K-major operand of N rows whose K
@@ -246,29 +256,45 @@ struct TileCursor {
 // hi = e4m3(q 2^sh), lo = e4m3((q 2^sh - hi) 16) with a power of two 2^sh per
 // head.  FP8 queries: the bytes as they are, multiplier q_scale (rows past HG
 // stay zero).  Thread -> head tid / TPH, dims [DPT (tid % TPH), + DPT).
-template <int HG, bool kQ8>
+template <int HG, bool kQ8, bool kRope>
 struct QueryBuild {
   static constexpr int TPH = kSmxThreads / HG;           // threads per head
   static constexpr int DPT = kD / TPH;                    // dims per thread
   static constexpr int NV = kQ8 ? DPT / 16 : DPT / 8;     // 16-byte loads per thread
+  static constexpr int NR = kRope ? (HG < 16 ? 16 : HG) : 0;   // RoPE operand rows (zero past HG)
   uint4 v[NV];
+  uint4 rv;                                               // RoPE: 8 dims of head tid / 8
   float qs;                                               // FP8 queries: q_scale of the head
 
   __device__ __forceinline__ void load(const AttnArgs& a, int t, int h0) {
     const int head = threadIdx.x / TPH, part = threadIdx.x % TPH;
     const int64_t th = (int64_t)t * a.H + h0 + head;
     const uint4* src = kQ8 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + th * kD + part * DPT)
-                           : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * kD + part * DPT);
+                           : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * a.q_row + part * DPT);
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
     qs = kQ8 ? __ldg(a.q_scale + th) : 0.f;
+    if constexpr (kRope) {
+      const int rh = threadIdx.x >> 3, rc = threadIdx.x & 7;   // head, 16-byte chunk of its 64 dims
+      rv = make_uint4(0, 0, 0, 0);
+      if (rh < HG) {
+        const uint16_t* qr = static_cast<const uint16_t*>(a.q) + ((int64_t)t * a.H + h0 + rh) * a.q_row + kD;
+        rv = __ldg(reinterpret_cast<const uint4*>(qr) + rc);
+      }
+    }
   }
 
-  // Writes the operand into qbuf (NQ rows) and the multipliers into qsig.
+  // Writes the operand into qbuf (NQ rows), the multipliers into qsig and,
+  // for 656-byte rows, the BF16 RoPE operand (NR rows x 64 dims) into rbuf.
   template <int NQ>
-  __device__ __forceinline__ void store(const AttnArgs& a, uint8_t* qbuf, float* qsig) const {
+  __device__ __forceinline__ void store(const AttnArgs& a, uint8_t* qbuf, float* qsig, uint8_t* rbuf) const {
     const int head = threadIdx.x / TPH, part = threadIdx.x % TPH;
     const float base_sig = a.sm_scale * kLog2e;
+    if constexpr (kRope) {
+      const int rh = threadIdx.x >> 3, rc = threadIdx.x & 7;
+      if (rh < NR)
+        *reinterpret_cast<uint4*>(rbuf + (rh >> 3) * 1024 + (rh & 7) * 128 + ((rc ^ (rh & 7)) << 4)) = rv;
+    }
     if constexpr (kQ8) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(head, part * DPT + 16 * i)) = v[i];
@@ -330,9 +356,9 @@ struct QueryBuild {
 // Index warp: per tile, the physical rows of the 128 top-k entries (lane l
 // owns entries 4l .. 4l + 3) into the ring and the valid bits into the
 // tile's stage.
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0, int n_it) {
-  using C = Cfg<HG, kScaled, kQ8>;
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
   constexpr int kAhead = 3;
   const int lane = threadIdx.x & 31;
   volatile int* abort = &ms.abort;
@@ -428,11 +454,11 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
 // Producers: copy the rows of each tile into its stage.  Warp pw owns tile
 // rows [64 pw, 64 pw + 64); one warp instruction moves 128-byte piece kb of
 // four rows (lane: row 4g + lane / 8, 16-byte chunk lane % 8).
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it) {
-  using C = Cfg<HG, kScaled, kQ8>;
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
   constexpr int kRowsPerWarp = kRows / kProdWarps;   // 64
-  constexpr int R = kScaled ? kScaledRow : kRawRow;
+  constexpr int R = kRope ? kRopeRow : kScaled ? kScaledRow : kRawRow;
   const int ptid = threadIdx.x - kProdWarp0 * 32;
   const int pw = ptid >> 5, lane = ptid & 31;
   const int rq = lane >> 3, ch = lane & 7;
@@ -452,6 +478,7 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
     }
     mbar_arrive(smem_u32(&ms.idx_free[slot]));
     const uint32_t base = kv0 + stage * kStage;
+    const uint32_t rope_base = smem_u32(sm + C::ROPE_OFF) + stage * C::ROPE_STAGE;
 #pragma unroll
     for (int g = 0; g < kRowsPerWarp / 4; ++g) {
       const int r = kRowsPerWarp * pw + 4 * g + rq;
@@ -461,13 +488,16 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
       const uint32_t dst = base + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) cp_async_16_zfill(dst + kb * 16384, src + kb * 128, n);
+      if (kRope)   // the row's 64 BF16 RoPE dims: one 128-byte swizzled row of the RoPE tile
+        cp_async_16_zfill(rope_base + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4),
+                          src + kScaledRow, n);
     }
     if (kScaled) {
 #pragma unroll
       for (int k = 0; k < kRowsPerWarp / 32; ++k) {
         const int r = kRowsPerWarp * pw + 32 * k + lane;
         cp_async_16_zfill(smem_u32(sm + C::SC_OFF + stage * kScStage + r * 16),
-                          a.pool + (int64_t)(sc_rows[k] >= 0 ? sc_rows[k] : 0) * kScaledRow + kD,
+                          a.pool + (int64_t)(sc_rows[k] >= 0 ? sc_rows[k] : 0) * R + kD,
                           sc_rows[k] >= 0 ? 16u : 0u);
       }
     }
@@ -476,9 +506,9 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
   cp_async_wait_all();
 }
 
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 __device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it) {
-  using C = Cfg<HG, kScaled, kQ8>;
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
   if ((threadIdx.x & 31) != 0) return;
   volatile int* abort = &ms.abort;
   const uint32_t kv0 = smem_u32(sm + C::KV_OFF);
@@ -486,6 +516,9 @@ __device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem
   const uint32_t p0 = smem_u32(sm + C::P_OFF);
   constexpr uint32_t kIdQK = idesc_e4m3(C::NQ, false);
   constexpr uint32_t kIdPV = idesc_e4m3(C::NP, true);
+  constexpr uint32_t kIdRope = idesc_bf16(C::NR > 0 ? C::NR : 16);
+  const uint32_t rope0 = smem_u32(sm + C::ROPE_OFF);
+  const uint32_t qr0 = smem_u32(sm + C::QR_OFF);
   // Issue whichever is ready: PV of the oldest tile whose P is written, or
   // the next QK^T chunk whose tile, query and score buffer are in place.
   int qk_it = 0, qk_qc = 0, pv_j = 0, seg = -1;
@@ -546,6 +579,15 @@ __device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem
           const uint32_t acc = kScaled ? (kk > 0 ? 1u : 0u) : (ks > 0 ? 1u : 0u);
           mma_e4m3(d, ad, bd, kIdQK, acc);
         }
+        if (kRope && qk_qc == 0) {
+          // S_rope = K_rope Q_rope^T: 64 BF16 dims, K = 16 per MMA
+          const uint32_t ra = rope0 + stage * C::ROPE_STAGE;
+          const uint32_t rb = qr0 + (seg % C::NQB) * C::QR_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d_base + C::GC * C::NQ, sdesc_sw128(ra + kk * 32, 16, 1024), sdesc_sw128(rb + kk * 32, 16, 1024),
+                     kIdRope, kk > 0 ? 1u : 0u);
+        }
         mma_commit(smem_u32(&ms.s_full[sb]));
         if (++qk_qc == C::NQC) {
           qk_qc = 0;
@@ -603,10 +645,10 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)
   }
 }
 
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it,
                              int cta) {
-  using C = Cfg<HG, kScaled, kQ8>;
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
   constexpr int HPT = C::HPT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, hh = warp >> 2;
@@ -620,9 +662,9 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   int seg = -1;
   bool ok = true;                  // false once a wait gave up: keep going through every barrier
   TileCursor cur(a, b0);
-  QueryBuild<HG, kQ8> qnext;       // the next segment's query, loaded ahead of its build
+  QueryBuild<HG, kQ8, kRope> qnext;   // the next segment's query, loaded ahead of its build
   qnext.load(a, cur.t, cur.hgi * a.hg);
-  qnext.template store<C::NQ>(a, sm + C::Q_OFF, ms.qsig[0]);
+  qnext.template store<C::NQ>(a, sm + C::Q_OFF, ms.qsig[0], sm + C::QR_OFF);
   fence_proxy_async_smem();
   mbar_arrive(smem_u32(&ms.q_full[0]));
   for (int it = 0; it < n_it; ++it, cur.advance(a)) {
@@ -673,6 +715,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
           if (!kQ8) v = fmaf(__uint_as_float(lo[k]), ms.qsig[qb][HG + hbase + k], v);
           s2[k] = kScaled ? fmaf(sc4[g], v, s2[k]) : v;
         }
+      }
+      if (kRope && qc == 0) {
+        uint32_t rv[HPT];
+        tmem_ld_cols<HPT>(lane_base + sb * C::S_COLS + C::GC * C::NQ + hbase, rv);
+        tmem_wait_ld();
+        const float rsig = a.sm_scale * kLog2e;
+#pragma unroll
+        for (int k = 0; k < HPT; ++k) s2[k] = fmaf(__uint_as_float(rv[k]), rsig, s2[k]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&ms.s_free[sb]));
@@ -795,7 +845,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     // multipliers, and QK^T of this tile (the last reader of the operand) is done
     if (build_next) {
       const int nqb = (seg + 1) % C::NQB;
-      qnext.template store<C::NQ>(a, sm + C::Q_OFF + nqb * C::Q_BYTES, ms.qsig[nqb]);
+      qnext.template store<C::NQ>(a, sm + C::Q_OFF + nqb * C::Q_BYTES, ms.qsig[nqb], sm + C::QR_OFF + nqb * C::QR_BYTES);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&ms.q_full[nqb]));
     }
@@ -857,9 +907,9 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 }
 
 // 12 warps: three share a sub-partition's 16K registers, so at most 168 each.
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ AttnArgs a) {
-  using C = Cfg<HG, kScaled, kQ8>;
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Misc& ms = *reinterpret_cast<Misc*>(sm + C::MISC_OFF);
@@ -895,7 +945,7 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
   }
   // the query and P operands start zeroed: their padding rows (N rounded up
   // to 16) stay zero
-  for (int i = tid; i < (C::NQB * C::Q_BYTES + C::NPB * C::P_BYTES) / 16; i += kThreads)
+  for (int i = tid; i < (C::NQB * (C::Q_BYTES + C::QR_BYTES) + C::NPB * C::P_BYTES) / 16; i += kThreads)
     reinterpret_cast<uint4*>(sm + C::Q_OFF)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < 2 * 64; i += kThreads) (&ms.qsig[0][0])[i] = 0.f;
   fence_proxy_async_smem();
@@ -911,13 +961,13 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
   grid_launch_dependents();
 
   if (warp < kSmxWarps)
-    softmax_role<HG, kScaled, kQ8>(a, sm, ms, tmem, b0, n_it, cta);
+    softmax_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it, cta);
   else if (warp == kMmaWarp)
-    mma_role<HG, kScaled, kQ8>(a, sm, ms, tmem, b0, n_it);
+    mma_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it);
   else if (warp == kIdxWarp)
-    index_role<HG, kScaled, kQ8>(a, sm, ms, b0, n_it);
+    index_role<HG, kScaled, kQ8, kRope>(a, sm, ms, b0, n_it);
   else
-    producer_role<HG, kScaled, kQ8>(a, sm, ms, n_it);
+    producer_role<HG, kScaled, kQ8, kRope>(a, sm, ms, n_it);
 
   tc_fence_before();
   __syncthreads();
@@ -928,15 +978,15 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
   if (tid == 0 && ms.abort) set_err(a.err, DSA_DEV_ERR_TIMEOUT);
 }
 
-template <int HG, bool kScaled, bool kQ8>
+template <int HG, bool kScaled, bool kQ8, bool kRope>
 void launch_tc(const AttnArgs& a, cudaStream_t stream) {
-  using C = Cfg<HG, kScaled, kQ8>;
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(sparse_attn_tc_kernel<HG, kScaled, kQ8>,
+    if (cudaFuncSetAttribute(sparse_attn_tc_kernel<HG, kScaled, kQ8, kRope>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return;   // the launch below is skipped; the caller sees the attribute error
     configured.fetch_or(bit);
@@ -953,15 +1003,22 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<HG, kScaled, kQ8>, a);
+  cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<HG, kScaled, kQ8, kRope>, a);
 }
 
 template <int HG>
 void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
-  if (q8 && a.scaled) launch_tc<HG, true, true>(a, stream);
-  else if (q8) launch_tc<HG, false, true>(a, stream);
-  else if (a.scaled) launch_tc<HG, true, false>(a, stream);
-  else launch_tc<HG, false, false>(a, stream);
+  if (a.rope) {
+    if constexpr (HG <= 16) launch_tc<HG, true, false, true>(a, stream);   // host checks H
+  } else if (q8 && a.scaled) {
+    launch_tc<HG, true, true, false>(a, stream);
+  } else if (q8) {
+    launch_tc<HG, false, true, false>(a, stream);
+  } else if (a.scaled) {
+    launch_tc<HG, true, false, false>(a, stream);
+  } else {
+    launch_tc<HG, false, false, false>(a, stream);
+  }
   if (a.ws_o != nullptr) launch_combine(a, stream);
 }
 

@@ -69,7 +69,8 @@ def prefill(L, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(D=576), 4), (dict(kvd=528), 4), (dict(layout=2), 3), (dict(K=0), 5), (dict(K=2000), 5),
+    (dict(D=576), 4), (dict(kvd=528), 4), (dict(layout=3), 3), (dict(layout=2), 4),
+    (dict(layout=2, D=576, kvd=576, H=32), 6), (dict(K=0), 5), (dict(K=2000), 5),
     (dict(H=12), 6), (dict(H=256), 6), (dict(T=-1), 2), (dict(q=None), 1), (dict(pool=None), 1),
     (dict(topk=None), 1), (dict(o=None), 1), (dict(lse=None), 1), (dict(rows=0), 2),
     (dict(pt=FAKE, B=0), 2), (dict(pt=FAKE, ps=0), 2), (dict(q=FAKE + 8), 10), (dict(o=FAKE + 4), 10),
@@ -80,7 +81,7 @@ def test_decode_host_validation(L, kw, code):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(layout=2), 3), (dict(layout=-1), 3), (dict(qs=None), 1), (dict(D=1024), 4), (dict(K=64), 5), (dict(H=7), 6),
+    (dict(layout=2, D=576, kvd=576), 3), (dict(layout=3), 3), (dict(layout=-1), 3), (dict(qs=None), 1), (dict(D=1024), 4), (dict(K=64), 5), (dict(H=7), 6),
 ])
 def test_prefill_host_validation(L, kw, code):
     assert prefill(L, **kw) == code

@@ -107,6 +107,21 @@ def test_prefill_q8_scaled528(T, full):
     assert_attn_close(O, L, Or, Lr, f"prefill_q8_scaled528 T={T}")
 
 
+@pytest.mark.parametrize("T,K,H,full", [(16, 512, 16, True), (8, 256, 8, True), (64, 2048, 16, False)])
+def test_decode_rope656(T, K, H, full):
+    """656-byte rows: group-scaled latent plus 64 BF16 RoPE dims; 576-wide
+    queries and keys (the RoPE scores by BF16 MMAs), 512-wide values."""
+    w = W.decode_rope656(T=T, K=K, H=H, pool_rows=131072 if not full else 16384)
+    pool, pd = pool_for(w, ("rope", T, K, H))
+    O, L, err = run_decode(w, pd)
+    tok = None if full else sample_tokens(T, 16, 10)
+    Or, Lr, _ = oracle_decode(w, pool, tokens=tok)
+    assert err == 0
+    if tok is not None:
+        O, L = O[tok], L[tok]
+    assert_attn_close(O, L, Or, Lr, f"decode_rope656 T={T} H={H}")
+
+
 def test_prefill_q8_short_context_padding():
     """Zero prior context: early tokens have fewer than K causal rows, so the
     list is padded with -1 (down to a single valid entry for the first token)."""

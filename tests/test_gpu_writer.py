@@ -21,7 +21,8 @@ def _finite_bf16_patterns(include_inf: bool) -> np.ndarray:
 def _write_gpu(layout, x_bits, slots, pool_init):
     pool = dev(pool_init.copy())
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fn = binding.dsa_kv_write_raw if layout == "raw512" else binding.dsa_kv_write_scaled
+    fn = {"raw512": binding.dsa_kv_write_raw, "scaled528": binding.dsa_kv_write_scaled,
+          "rope656": binding.dsa_kv_write_rope656}[layout]
     fn(bf16_dev(x_bits), dev(slots.astype(np.int64)), pool, err_flag=err)
     torch.cuda.synchronize()
     return pool.cpu().numpy(), int(err.item())
@@ -75,6 +76,33 @@ def test_writer_slot_edge_cases(layout):
     got, err = _write_gpu(layout, x, slots, init)
     assert err == binding.DSA_DEV_ERR_SLOT_RANGE
     assert np.array_equal(got, ref)
+
+
+def test_rope656_writer_bit_exact():
+    """656-byte rows: 8192 rows of the decode_rope656 source (latent N(0,1)*U(0.1,4),
+    RoPE N(0,1)) plus rows of every finite BF16 pattern in both parts, into
+    random slots; a skipped and an out-of-range slot."""
+    w = W.decode_rope656(T=1, K=128, pool_rows=8192)
+    rng = np.random.default_rng(102)
+    bits = _finite_bf16_patterns(include_inf=False)
+    bits = bits[rng.permutation(bits.size)]
+    n_extra = -(-bits.size // 576)
+    extra = np.zeros(n_extra * 576, dtype=np.uint16)
+    extra[: bits.size] = bits
+    x = np.concatenate([w["kv_src"], extra.reshape(n_extra, 576)])
+    n = x.shape[0]
+    slots = rng.permutation(n + 9)[:n].astype(np.int64)
+    slots[5] = -1
+    init = np.full((n + 9, 656), 0x3C, dtype=np.uint8)
+    ok = slots.copy()
+    slots[7] = n + 50                                        # beyond the pool: flagged, not written
+    ok[7] = -1
+    ref = init.copy()
+    oracle.kv_write("rope656", x, ok, ref)
+    got, err = _write_gpu("rope656", x, slots, init)
+    assert err == binding.DSA_DEV_ERR_SLOT_RANGE
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:3].tolist()}"
 
 
 def test_writer_empty_is_noop():
