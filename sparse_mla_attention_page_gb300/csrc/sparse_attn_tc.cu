@@ -11,17 +11,16 @@
 //              tiles ahead, page-table reads one tile ahead, so no load
 //              latency sits between tiles), publishes them in a ring of
 //              kRing tiles for the producers together with the tile's
-//              valid-entry bits, and fetches the FP8 query operand of each
-//              new segment with one bulk copy (prepared by
-//              prep_query_kernel, which runs first).
+//              valid-entry bits.
 //   producer   2 warps: gather each tile's rows with 16-byte cp.async into
 //              the 128-byte-swizzled K-major tile, four rows x 128 bytes per
 //              warp instruction (whole 128-byte lines), zero-filling masked
-//              entries (source size 0: no memory read); a stage is complete
-//              when every producer thread's copies have landed
+//              entries (source size 0: no memory read); 656-byte rows also
+//              bring their 128-byte RoPE part into a tile of its own; a stage
+//              is complete when every producer thread's copies have landed
 //              (cp.async.mbarrier.arrive.noinc).  (Row gathers through the
-//              tensor memory accelerator, tile::gather4, move 128 bytes per
-//              request and top out near a quarter of HBM bandwidth per SM.)
+//              tensor memory accelerator, tile::gather4, are issue-bound and
+//              ran slower than cp.async here.)
 //   MMA        1 thread: S^T = K Q^T (M = 128 rows, N = query columns, K = 512)
 //              and O^T += V^T P^T (M = 128 latent dims x 4, N = P columns,
 //              K = 128 rows), both kind::f8f6f4 with FP32 accumulators in
@@ -30,14 +29,18 @@
 //              ~64 cycles for any N up to 128, so the pipe must never wait on
 //              one queue while the other is ready).  The same shared-memory tile is
 //              the K-major A operand of the first and the MN-major A operand
-//              of the second (V = K: one absorbed NoPE latent row).
+//              of the second (V = K: one absorbed NoPE latent row).  Over
+//              656-byte rows, four kind::f16 MMAs per tile add the BF16 RoPE
+//              scores K_rope Q_rope^T in extra score columns.
 //   softmax    8 warps, two per TMEM lane quarter, each thread one tile row
 //              (= TMEM lane) and half of the heads: combine the
 //              score columns, mask, reduce the tile max per head across the
 //              128 rows, keep a lazy running max (O in TMEM is rescaled only
 //              when the max grows by more than 2^8), form p = 2^(s - m),
-//              accumulate the denominators, write P as an FP8 operand, and at
-//              the end of a segment normalise O and store it (a unit whose
+//              accumulate the denominators, write P as an FP8 operand, build
+//              each segment's query operand in shared memory (loads issued a
+//              tile ahead), and at the end of a segment normalise O and store
+//              it (a unit whose
 //              tiles span CTAs leaves a normalised partial O and LSE per CTA;
 //              combine_kernel, launched right behind as a programmatic
 //              dependent, merges them).
