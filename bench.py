@@ -324,33 +324,60 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
 
-    # end to end through the public API: inputs from pinned host memory, results back
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_q = pin(w["q_bf16"].view(np.int16)).view(torch.bfloat16)
-    h_topk = pin(w["topk"])
-    h_pt = None if w["page_table"] is None else pin(w["page_table"])
-    h_x = pin(x_new_h.view(np.int16)).view(torch.bfloat16)
-    h_slots = pin(slots_h)
-    h_o = torch.empty(T, H, 512, dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty(T, H, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_topk, h_x, h_slots) + ((h_pt,) if h_pt is not None else ()))
-    d2h = h_o.numel() * 2 + h_lse.numel() * 4
+    # end to end through the public API: the step's inputs from one pinned host
+    # buffer (one H2D copy), the results back in one D2H copy
+    def packed(parts):
+        """Byte offsets of 256-byte-aligned parts in one buffer, and its size."""
+        offs, n = [], 0
+        for a in parts:
+            offs.append(n)
+            n += (a.nbytes + 255) // 256 * 256
+        return offs, n
+
+    in_parts = [np.ascontiguousarray(w["q_bf16"]), np.ascontiguousarray(w["topk"]),
+                np.ascontiguousarray(x_new_h), np.ascontiguousarray(slots_h)]
+    if w["page_table"] is not None:
+        in_parts.append(np.ascontiguousarray(w["page_table"]))
+    in_offs, in_n = packed(in_parts)
+    h_in = torch.empty(in_n, dtype=torch.uint8).pin_memory()
+    for a, off in zip(in_parts, in_offs):
+        h_in[off:off + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
+    d_in = torch.empty(in_n, dtype=torch.uint8, device=dev)
+
+    def view(buf, off, a_shape, dtype):
+        n = int(np.prod(a_shape)) * torch.empty(0, dtype=dtype).element_size()
+        return buf[off:off + n].view(dtype).view(*a_shape)
+
+    q_e = view(d_in, in_offs[0], w["q_bf16"].shape, torch.bfloat16)
+    topk_e = view(d_in, in_offs[1], w["topk"].shape, torch.int32)
+    x_e = view(d_in, in_offs[2], x_new_h.shape, torch.bfloat16)
+    slots_e = view(d_in, in_offs[3], slots_h.shape, torch.int64)
+    pt_e = None if w["page_table"] is None else view(d_in, in_offs[4], w["page_table"].shape, torch.int32)
+    (o_off, lse_off), out_n = packed([np.empty((T, H, 512), np.uint16), np.empty((T, H), np.float32)])
+    d_out = torch.empty(out_n, dtype=torch.uint8, device=dev)
+    h_out = torch.empty(out_n, dtype=torch.uint8).pin_memory()
+    o_e = view(d_out, o_off, (T, H, 512), torch.bfloat16)
+    lse_e = view(d_out, lse_off, (T, H), torch.float32)
+    if prefill:
+        q8_e = torch.empty(T, H, 512, dtype=torch.uint8, device=dev)
+        qs_e = torch.empty(T, H, dtype=torch.float32, device=dev)
+    h2d, d2h = in_n, out_n
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
     for i in range(n_e2e + 3):
         flush_buf.zero_()
         if i >= 3:
             e2e_ev[i - 3][0].record(stream)
-        q.copy_(h_q, non_blocking=True)
-        topk.copy_(h_topk, non_blocking=True)
-        if pt is not None:
-            pt.copy_(h_pt, non_blocking=True)
-        x_new.copy_(h_x, non_blocking=True)
-        slots.copy_(h_slots, non_blocking=True)
-        step_write()
-        step_attn()
-        h_o.copy_(o, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        write(x_e, slots_e, pool)
+        if prefill:
+            binding.dsa_quantize_q8(q_e, q8_e, qs_e)
+            binding.dsa_sparse_attn_prefill_q8(q8_e, qs_e, pool, layout, topk_e, w["sm_scale"], o_e, lse_e, ws,
+                                               page_table=pt_e, page_size=w["page_size"])
+        else:
+            binding.dsa_sparse_attn_decode(q_e, pool, layout, topk_e, w["sm_scale"], o_e, lse_e, ws,
+                                           page_table=pt_e, page_size=w["page_size"])
+        h_out.copy_(d_out, non_blocking=True)
         if i >= 3:
             e2e_ev[i - 3][1].record(stream)
     torch.cuda.synchronize(dev)
