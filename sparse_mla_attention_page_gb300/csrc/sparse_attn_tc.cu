@@ -121,7 +121,14 @@ struct Cfg {
   // 656-byte rows: the RoPE part of the scores, S_rope = K_rope Q_rope^T (BF16
   // MMAs, N = NR query rows), accumulated in NR more columns of each score buffer
   static constexpr int NR = kRope ? (HG < 16 ? 16 : HG) : 0;
-  static constexpr int GC = (G * NQ + NR + O_COLS <= 512) ? G : G / 2;   // groups per QK^T chunk
+  // groups per QK^T chunk: the widest chunk for which two score buffers fit
+  // beside O (so QK^T of the next chunk overlaps the read-out of this one),
+  // else the widest that fits once
+  static constexpr int GC = (2 * (G * NQ + NR) + O_COLS <= 512)       ? G
+                            : (G >= 2 && 2 * (G / 2 * NQ + NR) + O_COLS <= 512) ? G / 2
+                            : (G >= 4 && 2 * (G / 4 * NQ + NR) + O_COLS <= 512) ? G / 4
+                            : (G * NQ + NR + O_COLS <= 512)             ? G
+                                                                        : G / 2;
   static constexpr int NQC = G / GC;                          // QK^T chunks per tile
   static constexpr int S_COLS = GC * NQ + NR;
   static constexpr int NS = (2 * S_COLS + O_COLS <= 512) ? 2 : 1;
