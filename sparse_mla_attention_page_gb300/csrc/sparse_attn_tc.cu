@@ -433,6 +433,12 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
   for (int it = 0; it < n_it; ++it) {
     int32_t rows[4];
     finish(pv, poff, rows);
+    // publish the rows first: the producers wait for them, nothing here waits
+    // for the loads of later tiles still in flight
+    const int slot = it % kRing, stage = it % C::NST;
+    if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort)) break;
+    *reinterpret_cast<int4*>(&ms.ring[slot][4 * lane]) = make_int4(rows[0], rows[1], rows[2], rows[3]);
+    mbar_arrive(smem_u32(&ms.idx_full[slot]));
     // entries of tile it + 1 + kAhead; page-table reads of tile it + 1
     const int4 nxt = win[0];
     const int nxt_sq = wseq[0];
@@ -443,11 +449,6 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
     }
     load_entries(it + 1 + kAhead, win[kAhead - 1], wseq[kAhead - 1]);
     issue(nxt, nxt_sq, pv, poff);
-
-    const int slot = it % kRing, stage = it % C::NST;
-    if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort)) break;
-    *reinterpret_cast<int4*>(&ms.ring[slot][4 * lane]) = make_int4(rows[0], rows[1], rows[2], rows[3]);
-    mbar_arrive(smem_u32(&ms.idx_full[slot]));
     // valid bits of the stage: it was released by PV(it - NST), which needed
     // the softmax to be done with the stage's previous tile
     if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort)) break;
