@@ -142,8 +142,13 @@ struct Cfg {
   static constexpr int QR_BYTES = NR * 128;                    // RoPE query operand
   static constexpr int STAGE = kStage + (kScaled ? kScStage : 0) + ROPE_STAGE;
   static constexpr int FIXED = kMiscBytes + 1024;             // + alignment slack
-  // shared memory: two P buffers first, then a third KV stage, then a second query buffer
-  static constexpr int NPB = (2 * STAGE + Q_BYTES + 2 * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
+  // shared memory: three KV stages and two P buffers if they fit; else, with
+  // one score group, three stages and one P buffer (the softmax forms P in
+  // registers and waits for the previous PV only to store it); else two P
+  // buffers; then a second query buffer
+  static constexpr bool kFit3x2 = 3 * STAGE + Q_BYTES + 2 * P_BYTES + FIXED <= kSmemLimit;
+  static constexpr bool kFit3x1 = G == 1 && 3 * STAGE + Q_BYTES + P_BYTES + FIXED <= kSmemLimit;
+  static constexpr int NPB = kFit3x2 ? 2 : kFit3x1 ? 1 : (2 * STAGE + Q_BYTES + 2 * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
   static constexpr int NST = (3 * STAGE + Q_BYTES + NPB * P_BYTES + FIXED <= kSmemLimit) ? 3 : 2;
   static constexpr int NQB =
       (NST * STAGE + 2 * (Q_BYTES + QR_BYTES) + NPB * P_BYTES + FIXED <= kSmemLimit) ? 2 : 1;
@@ -818,8 +823,10 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       }
       tmem_wait_st();
     }
-    // this P buffer was last read by PV(it - NPB)
-    if (it >= C::NPB) ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), ((it / C::NPB) - 1) & 1, abort);
+    // this P buffer was last read by PV(it - NPB); with a single buffer the
+    // wait comes after P is formed in registers, just before it is stored
+    constexpr bool kLateWait = C::NPB == 1 && C::G == 1;
+    if (!kLateWait && it >= C::NPB) ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), ((it / C::NPB) - 1) & 1, abort);
     const uint32_t pbuf = smem_u32(sm + C::P_OFF + pb * C::P_BYTES);
     // p = 2^(s - m) (0 while the head has seen no valid entry), denominators, P operand
 #pragma unroll
@@ -827,26 +834,41 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       s2[h] = m_run[h] == -INFINITY ? 0.f : ex2_approx(s2[h] - m_run[h]);
       l_part[h] += s2[h];
     }
+    // three E4M3 terms of a pair of P values: v ~ hi + mid / 16 + lo / 256
+    auto split = [](float v0, float v1, uint32_t& hi2, uint32_t& mid2, uint32_t& lo2) {
+      hi2 = e4m3x2_satrne(v0, v1);
+      const float2 hf = e4m3x2_to_f32x2(hi2);
+      const float r0 = (v0 - hf.x) * 16.f, r1 = (v1 - hf.y) * 16.f;
+      mid2 = e4m3x2_satrne(r0, r1);
+      const float2 mf = e4m3x2_to_f32x2(mid2);
+      lo2 = e4m3x2_satrne((r0 - mf.x) * 16.f, (r1 - mf.y) * 16.f);
+    };
+    auto store = [&](uint32_t pg, int n, uint32_t hi2, uint32_t mid2, uint32_t lo2) {
+      st_shared_u8(pg + kmajor_off<C::NP>(n, row), hi2 & 0xFFu);
+      st_shared_u8(pg + kmajor_off<C::NP>(n + 1, row), (hi2 >> 8) & 0xFFu);
+      st_shared_u8(pg + kmajor_off<C::NP>(HG + n, row), mid2 & 0xFFu);
+      st_shared_u8(pg + kmajor_off<C::NP>(HG + n + 1, row), (mid2 >> 8) & 0xFFu);
+      st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n, row), lo2 & 0xFFu);
+      st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n + 1, row), (lo2 >> 8) & 0xFFu);
+    };
+    if constexpr (kLateWait) {
+      uint32_t hi2[HPT / 2], mid2[HPT / 2], lo2[HPT / 2];
 #pragma unroll
-    for (int g = 0; g < C::G; ++g) {
-      const float mul = kScaled ? (e_grp[g] == -1000 ? 0.f : scale_pow2(sc4[g], -e_grp[g])) : 1.f;
-      const uint32_t pg = pbuf + g * (C::NP * 128);
+      for (int h = 0; h < HPT; h += 2) split(s2[h], s2[h + 1], hi2[h / 2], mid2[h / 2], lo2[h / 2]);
+      if (it >= 1) ok &= mbar_wait(smem_u32(&ms.pv_done[0]), (it - 1) & 1, abort);
 #pragma unroll
-      for (int h = 0; h < HPT; h += 2) {
-        const float v0 = s2[h] * mul, v1 = s2[h + 1] * mul;
-        const uint32_t hi2 = e4m3x2_satrne(v0, v1);
-        const float2 hf = e4m3x2_to_f32x2(hi2);
-        const float r0 = (v0 - hf.x) * 16.f, r1 = (v1 - hf.y) * 16.f;
-        const uint32_t mid2 = e4m3x2_satrne(r0, r1);
-        const float2 mf = e4m3x2_to_f32x2(mid2);
-        const uint32_t lo2 = e4m3x2_satrne((r0 - mf.x) * 16.f, (r1 - mf.y) * 16.f);
-        const int n = hbase + h;
-        st_shared_u8(pg + kmajor_off<C::NP>(n, row), hi2 & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(n + 1, row), (hi2 >> 8) & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(HG + n, row), mid2 & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(HG + n + 1, row), (mid2 >> 8) & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n, row), lo2 & 0xFFu);
-        st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n + 1, row), (lo2 >> 8) & 0xFFu);
+      for (int h = 0; h < HPT; h += 2) store(pbuf, hbase + h, hi2[h / 2], mid2[h / 2], lo2[h / 2]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < C::G; ++g) {
+        const float mul = kScaled ? (e_grp[g] == -1000 ? 0.f : scale_pow2(sc4[g], -e_grp[g])) : 1.f;
+        const uint32_t pg = pbuf + g * (C::NP * 128);
+#pragma unroll
+        for (int h = 0; h < HPT; h += 2) {
+          uint32_t hi2, mid2, lo2;
+          split(s2[h] * mul, s2[h + 1] * mul, hi2, mid2, lo2);
+          store(pg, hbase + h, hi2, mid2, lo2);
+        }
       }
     }
     fence_proxy_async_smem();
