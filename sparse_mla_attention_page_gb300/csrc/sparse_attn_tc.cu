@@ -10,9 +10,10 @@
 //              page table into physical rows (top-k entries fetched three
 //              tiles ahead, page-table reads one tile ahead, so no load
 //              latency sits between tiles), publishes them in a ring of
-//              kRing tiles for the producers together with the tile's
-//              valid-entry bits.
-//   producer   2 warps: gather each tile's rows with 16-byte cp.async into
+//              kRing tiles for the producers; nothing ties it to the stages,
+//              so it runs up to kRing tiles ahead of them.
+//   producer   2 warps: publish a stage's valid-entry bits once the stage is
+//              free, then gather each tile's rows with 16-byte cp.async into
 //              the 128-byte-swizzled K-major tile, four rows x 128 bytes per
 //              warp instruction (whole 128-byte lines), zero-filling masked
 //              entries (source size 0: no memory read); 656-byte rows also
@@ -440,7 +441,7 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
     finish(pv, poff, rows);
     // publish the rows first: the producers wait for them, nothing here waits
     // for the loads of later tiles still in flight
-    const int slot = it % kRing, stage = it % C::NST;
+    const int slot = it % kRing;
     if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort)) break;
     *reinterpret_cast<int4*>(&ms.ring[slot][4 * lane]) = make_int4(rows[0], rows[1], rows[2], rows[3]);
     mbar_arrive(smem_u32(&ms.idx_full[slot]));
@@ -454,16 +455,6 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
     }
     load_entries(it + 1 + kAhead, win[kAhead - 1], wseq[kAhead - 1]);
     issue(nxt, nxt_sq, pv, poff);
-    // valid bits of the stage: it was released by PV(it - NST), which needed
-    // the softmax to be done with the stage's previous tile
-    if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort)) break;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const unsigned vm = __ballot_sync(0xffffffffu, rows[k] >= 0);
-      if (lane == 0) ms.vmask[stage][k] = vm;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&ms.meta_full[stage]));
   }
 }
 
@@ -493,6 +484,17 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
       for (int k = 0; k < kRowsPerWarp / 32; ++k) sc_rows[k] = ms.ring[slot][kRowsPerWarp * pw + 32 * k + lane];
     }
     mbar_arrive(smem_u32(&ms.idx_free[slot]));
+    // valid bits of the stage (its previous tile's softmax is done: PV of
+    // that tile released the stage): lane rq holds rows 4g + rq of this
+    // warp's half, i.e. bits 16 pw + g of word rq
+    {
+      uint32_t bits = 0;
+#pragma unroll
+      for (int g = 0; g < kRowsPerWarp / 4; ++g) bits |= (rows[g] >= 0 ? 1u : 0u) << g;
+      if (ch == 0) reinterpret_cast<uint16_t*>(&ms.vmask[stage][rq])[pw] = (uint16_t)bits;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ms.meta_full[stage]));
+    }
     const uint32_t base = kv0 + stage * kStage;
     const uint32_t rope_base = smem_u32(sm + C::ROPE_OFF) + stage * C::ROPE_STAGE;
 #pragma unroll
@@ -955,7 +957,7 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
     for (int s = 0; s < 3; ++s) {
       mbar_init(smem_u32(&ms.kv_full[s]), kProdWarps * 32);
       mbar_init(smem_u32(&ms.kv_empty[s]), 1);
-      mbar_init(smem_u32(&ms.meta_full[s]), 1);
+      mbar_init(smem_u32(&ms.meta_full[s]), kProdWarps);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(smem_u32(&ms.idx_full[s]), 32);
