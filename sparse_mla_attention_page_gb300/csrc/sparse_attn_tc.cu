@@ -755,50 +755,62 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
       for (int h = 0; h < HPT; ++h) s2[h] = -INFINITY;
     }
-    // tile maxima over the 128 rows: per head, and per scale group
+    // Does a head's running maximum have to grow?  Each thread tests its own
+    // row and one barrier ORs the answers; only then are the tile maxima
+    // formed (each segment's first tile and the rare tiles whose maximum
+    // exceeds the running one by more than 2^kTau).  528-byte rows also track
+    // the group-scale exponents; testing those per row cost more than the
+    // exchange it saves (measured), so their tiles always form the maxima.
+    bool grow = false;
+#pragma unroll
+    for (int h = 0; h < HPT; ++h) grow |= s2[h] > m_run[h] + kTau;
     float tmp[HPT];
-#pragma unroll
-    for (int h = 0; h < HPT; ++h) tmp[h] = s2[h];
-    const float wmax = transpose_reduce<HPT, true>(tmp, lane);
-    if (lane < HPT) ms.red[it & 1][hh][quarter][lane] = wmax;
-    if (kScaled && hh == 0) {
-      float sct[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) sct[g] = valid ? fabsf(sc4[g]) : 0.f;
-      const float wsc = transpose_reduce<4, true>(sct, lane);
-      if (lane < 4) ms.red_sc[it & 1][quarter][lane] = wsc;
-    }
-    named_bar_sync(1, kSmxThreads);
-    const int hl = lane % HPT;
-    const float tile_max = fmaxf(fmaxf(ms.red[it & 1][hh][0][hl], ms.red[it & 1][hh][1][hl]),
-                                 fmaxf(ms.red[it & 1][hh][2][hl], ms.red[it & 1][hh][3][hl]));
-    const bool need = tile_max > m_lane + kTau;
-    const unsigned rmask = __ballot_sync(0xffffffffu, need);
+    unsigned rmask = 0;
     float alpha_lane = 1.f;
-    if (need) {
-      alpha_lane = ex2_approx(m_lane - tile_max);
-      m_lane = tile_max;
-    }
-    if (rmask) {
-#pragma unroll
-      for (int h = 0; h < HPT; ++h) {
-        m_run[h] = __shfl_sync(0xffffffffu, m_lane, h);
-        l_part[h] *= __shfl_sync(0xffffffffu, alpha_lane, h);
-      }
-    }
     float beta[4] = {1.f, 1.f, 1.f, 1.f};
     bool bchange = false;
-    if (kScaled) {
+    if (kScaled || named_bar_red_or(1, kSmxThreads, grow)) {
+      // tile maxima over the 128 rows: per head, and per scale group
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float mx = fmaxf(fmaxf(ms.red_sc[it & 1][0][g], ms.red_sc[it & 1][1][g]),
-                               fmaxf(ms.red_sc[it & 1][2][g], ms.red_sc[it & 1][3][g]));
-        if (mx > 0.f && mx <= 3.0e38f) {
-          const int e = ceil_log2(mx);
-          if (e > e_grp[g]) {
-            beta[g] = e_grp[g] == -1000 ? 0.f : scale_pow2(1.f, e_grp[g] - e);
-            e_grp[g] = e;
-            bchange = true;
+      for (int h = 0; h < HPT; ++h) tmp[h] = s2[h];
+      const float wmax = transpose_reduce<HPT, true>(tmp, lane);
+      if (lane < HPT) ms.red[it & 1][hh][quarter][lane] = wmax;
+      if (kScaled && hh == 0) {
+        float sct[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) sct[g] = valid ? fabsf(sc4[g]) : 0.f;
+        const float wsc = transpose_reduce<4, true>(sct, lane);
+        if (lane < 4) ms.red_sc[it & 1][quarter][lane] = wsc;
+      }
+      named_bar_sync(1, kSmxThreads);
+      const int hl = lane % HPT;
+      const float tile_max = fmaxf(fmaxf(ms.red[it & 1][hh][0][hl], ms.red[it & 1][hh][1][hl]),
+                                   fmaxf(ms.red[it & 1][hh][2][hl], ms.red[it & 1][hh][3][hl]));
+      const bool need = tile_max > m_lane + kTau;
+      rmask = __ballot_sync(0xffffffffu, need);
+      if (need) {
+        alpha_lane = ex2_approx(m_lane - tile_max);
+        m_lane = tile_max;
+      }
+      if (rmask) {
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) {
+          m_run[h] = __shfl_sync(0xffffffffu, m_lane, h);
+          l_part[h] *= __shfl_sync(0xffffffffu, alpha_lane, h);
+        }
+      }
+      if (kScaled) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float mx = fmaxf(fmaxf(ms.red_sc[it & 1][0][g], ms.red_sc[it & 1][1][g]),
+                                 fmaxf(ms.red_sc[it & 1][2][g], ms.red_sc[it & 1][3][g]));
+          if (mx > 0.f && mx <= 3.0e38f) {
+            const int e = ceil_log2(mx);
+            if (e > e_grp[g]) {
+              beta[g] = e_grp[g] == -1000 ? 0.f : scale_pow2(1.f, e_grp[g] - e);
+              e_grp[g] = e;
+              bchange = true;
+            }
           }
         }
       }
