@@ -90,6 +90,20 @@ def test_prefill_q8_raw512(T, full):
     assert_attn_close(O, L, Or, Lr, f"prefill_q8 T={T}")
 
 
+@pytest.mark.parametrize("H", [8, 16, 64])
+def test_prefill_q8_head_counts(H):
+    """FP8 queries with 8 and 16 heads (one head group) and 64 heads (two groups of 32,
+    the one-P-buffer pipeline); a short context pads the first tokens' top-k with -1."""
+    w = W.prefill_q8_raw512(T=24, H=H, context=1024, pool_rows=2048)
+    pool, pd = pool_for(w, ("prefill_heads", H))
+    q8, qs = oracle.quantize_q8(w["q_bf16"])
+    O, L, err = run_prefill(w, pd, q8, qs)
+    Or, Lr, _ = oracle.sparse_attn(pool, "raw512", w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                                   page_table=w["page_table"])
+    assert err == 0
+    assert_attn_close(O, L, Or, Lr, f"prefill_q8 H={H}")
+
+
 @pytest.mark.parametrize("T,full", [(64, True), (4096, False)])
 def test_prefill_q8_scaled528(T, full):
     """FP8 queries over group-scaled 528-byte rows (beyond the pages, which keep
