@@ -62,8 +62,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=300)
-    p.add_argument("--op", choices=["attention", "gather_dequant"], default="attention",
-                   help="gather_dequant times the BF16 reader over the workload's top-k lists instead")
+    p.add_argument("--op", choices=["attention", "gather_dequant", "kv_write"], default="attention",
+                   help="gather_dequant times the BF16 reader over the workload's top-k lists instead; "
+                        "kv_write times one KV writer on 16384 new rows into a 262144-row pool")
+    p.add_argument("--layout", choices=["raw512", "scaled528", "rope656"], default="raw512",
+                   help="row layout of --op kv_write")
     return p.parse_args()
 
 
@@ -147,6 +150,51 @@ def run_gather(args) -> dict:
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "op": "gather_dequant", "T": T, "K": K, "layout": layout,
                        "valid_entries": valid, "l2": "flushed before every call"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "algorithmic_bytes_per_call": abytes}}
+
+
+def run_kv_write(args) -> dict:
+    """One fused BF16 -> FP8 KV writer on 16384 new rows (N(0,1) x U(0.1, 8)) into
+    distinct random slots of a 262144-row pool: CUDA events around each call,
+    L2 flushed before every call."""
+    import torch
+
+    from sparse_mla_attention_page_gb300 import binding
+    dev = torch.device("cuda", 0)
+    w = W.writer_rows()
+    layout, n = args.layout, w["n_rows"]
+    x = w["x_bf16"]
+    if layout == "rope656":   # 576-wide input rows: 512 latent dims + 64 RoPE dims
+        rope = W.f32_to_bf16_bits(W.rng_for(8).standard_normal((n, W.D_ROPE), dtype=np.float32))
+        x = np.concatenate([x, rope], axis=1)
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    slots = torch.from_numpy(w["slots"]).to(dev)
+    pool = torch.zeros(w["pool_rows"], ROW_BYTES[layout], dtype=torch.uint8, device=dev)
+    write = WRITERS[layout](binding)
+    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 256 << 20),
+                        dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        write(xd, slots, pool)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record()
+        write(xd, slots, pool)
+        ev[i][1].record()
+    torch.cuda.synchronize(dev)
+    us = float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) * 1e3
+    abytes = n * (x.shape[1] * 2 + ROW_BYTES[layout] + 8)     # BF16 row in, FP8 row out, slot
+    peak = float(measured_peaks().get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = abytes / (us * 1e-6) / 1e9
+    return {"metric": "KV writer rows/s and HBM GB/s (fraction of GB300 roofline)",
+            "value": round(n / (us * 1e-6), 1), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "us_per_call": round(us, 3), "higher_is_better": True,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"op": "kv_write", "layout": layout, "n_rows": n, "pool_rows": w["pool_rows"],
+                       "slots": "distinct, uniform over the pool", "l2": "flushed before every call"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "algorithmic_bytes_per_call": abytes}}
 
@@ -535,9 +583,9 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     import importlib
     importlib.import_module("sparse_mla_attention_page_gb300.build").build()
-    if args.op == "gather_dequant":
+    if args.op in ("gather_dequant", "kv_write"):
         if rank == 0:
-            print(json.dumps(run_gather(args)), flush=True)
+            print(json.dumps(run_gather(args) if args.op == "gather_dequant" else run_kv_write(args)), flush=True)
         return
     out = run_ours(args, rank, world, local_rank, dist)
     if out is not None:

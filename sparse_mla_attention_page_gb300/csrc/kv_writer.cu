@@ -45,22 +45,32 @@ __device__ __forceinline__ void allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(256) kv_write_raw_kernel(
+__global__ void __launch_bounds__(256, 4) kv_write_raw_kernel(
     const uint16_t* __restrict__ x, int64_t n_rows, const int64_t* __restrict__ slots,
     uint8_t* __restrict__ pool, int64_t pool_rows, int32_t* err) {
   allow_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n_rows; i += nwarps) {
-    const int64_t s = __ldg(slots + i);
-    if (s < 0) continue;
+  auto put = [&](int64_t s, const Row16& r) {
+    if (s < 0) return;
     if (s >= pool_rows) {
       if (lane == 0) set_err(err, DSA_DEV_ERR_SLOT_RANGE);
-      continue;
+      return;
     }
-    Row16 r;
-    load_row16(x + i * kD, lane, r);
     store_row16(pool + s * kRawRow, lane, r);
+  };
+  // two rows per warp and pass: both slots and both rows are loaded before
+  // either is used, so a pass costs one load round trip
+  for (int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i0 < n_rows; i0 += 2 * nwarps) {
+    const int64_t i1 = i0 + nwarps;
+    const bool two = i1 < n_rows;
+    const int64_t s0 = __ldg(slots + i0);
+    const int64_t s1 = two ? __ldg(slots + i1) : -1;
+    Row16 r0, r1;
+    load_row16(x + i0 * kD, lane, r0);
+    if (two) load_row16(x + i1 * kD, lane, r1);
+    put(s0, r0);
+    if (two) put(s1, r1);
   }
 }
 
@@ -69,7 +79,7 @@ __global__ void __launch_bounds__(256) kv_write_raw_kernel(
 // kRope: 656-byte rows, whose input rows are 576 wide; the 64 RoPE dims are
 // stored as they are (BF16) after the scales, one 4-byte pair per lane.
 template <bool kRope>
-__global__ void __launch_bounds__(256) kv_write_scaled_kernel(
+__global__ void __launch_bounds__(256, 4) kv_write_scaled_kernel(
     const uint16_t* __restrict__ x, int64_t n_rows, const int64_t* __restrict__ slots,
     uint8_t* __restrict__ pool, int64_t pool_rows, int32_t* err) {
   allow_dependents();
@@ -77,17 +87,12 @@ __global__ void __launch_bounds__(256) kv_write_scaled_kernel(
   constexpr int kRowBytes = kRope ? kRopeRow : kScaledRow;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n_rows; i += nwarps) {
-    const int64_t s = __ldg(slots + i);
-    if (s < 0) continue;
+  auto put = [&](int64_t s, Row16& r, uint32_t rope_pair) {
+    if (s < 0) return;
     if (s >= pool_rows) {
       if (lane == 0) set_err(err, DSA_DEV_ERR_SLOT_RANGE);
-      continue;
+      return;
     }
-    Row16 r;
-    load_row16(x + i * kIn, lane, r);
-    uint32_t rope_pair = 0;
-    if (kRope) rope_pair = __ldg(reinterpret_cast<const uint32_t*>(x + i * kIn + kD) + lane);
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -115,16 +120,31 @@ __global__ void __launch_bounds__(256) kv_write_scaled_kernel(
       float4 sc = make_float4(s0, g1, s1, g3);
       *reinterpret_cast<float4*>(row + 512) = sc;
     }
+  };
+  // two rows per warp and pass, all loads issued before any is used
+  for (int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i0 < n_rows; i0 += 2 * nwarps) {
+    const int64_t i1 = i0 + nwarps;
+    const bool two = i1 < n_rows;
+    const int64_t s0 = __ldg(slots + i0);
+    const int64_t s1 = two ? __ldg(slots + i1) : -1;
+    Row16 r0, r1;
+    load_row16(x + i0 * kIn, lane, r0);
+    if (two) load_row16(x + i1 * kIn, lane, r1);
+    uint32_t p0 = 0, p1 = 0;
+    if (kRope) {
+      p0 = __ldg(reinterpret_cast<const uint32_t*>(x + i0 * kIn + kD) + lane);
+      if (two) p1 = __ldg(reinterpret_cast<const uint32_t*>(x + i1 * kIn + kD) + lane);
+    }
+    put(s0, r0, p0);
+    if (two) put(s1, r1, p1);
   }
 }
 
-__global__ void __launch_bounds__(256) quantize_q8_kernel(
+__global__ void __launch_bounds__(256, 4) quantize_q8_kernel(
     const uint16_t* __restrict__ q, int64_t n_vec, uint8_t* __restrict__ q8, float* __restrict__ scale) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n_vec; i += nwarps) {
-    Row16 r;
-    load_row16(q + i * kD, lane, r);
+  auto put = [&](int64_t i, Row16& r) {
     float a = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(r.v[k]));
@@ -134,13 +154,25 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(
     for (int k = 0; k < 16; ++k) r.v[k] = s == 0.f ? 0.f : __fdiv_rn(r.v[k], s);
     store_row16(q8 + i * kD, lane, r);
     if (lane == 0) scale[i] = s;
+  };
+  // two vectors per warp and pass, both loaded before either is used
+  for (int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i0 < n_vec; i0 += 2 * nwarps) {
+    const int64_t i1 = i0 + nwarps;
+    const bool two = i1 < n_vec;
+    Row16 r0, r1;
+    load_row16(q + i0 * kD, lane, r0);
+    if (two) load_row16(q + i1 * kD, lane, r1);
+    put(i0, r0);
+    if (two) put(i1, r1);
   }
 }
 
+// Two rows per warp and pass, eight warps per block; at most one wave of
+// four blocks per SM (the kernels are built for four resident blocks).
 int writer_grid(int64_t n_rows, int sms) {
-  const int64_t warps_per_block = 8;
-  int64_t blocks = (n_rows + warps_per_block - 1) / warps_per_block;
-  const int64_t cap = (int64_t)sms * 16;
+  const int64_t rows_per_block = 16;
+  int64_t blocks = (n_rows + rows_per_block - 1) / rows_per_block;
+  const int64_t cap = (int64_t)sms * 4;
   if (blocks > cap) blocks = cap;
   return (int)(blocks < 1 ? 1 : blocks);
 }
