@@ -66,15 +66,18 @@ def parse_args():
                    help="gather_dequant times the BF16 reader over the workload's top-k lists instead; "
                         "kv_write times one KV writer on 16384 new rows into a 262144-row pool")
     p.add_argument("--layout", choices=["raw512", "scaled528", "rope656"], default="raw512",
-                   help="row layout of --op kv_write")
+                   help="row layout of --op kv_write and of --workload writer_sweep (raw512, scaled528)")
+    p.add_argument("--heads", type=int, default=16, help="head count of --workload writer_sweep")
     return p.parse_args()
 
 
 # ----------------------------------------------------------------- workloads
 
-def make_workload(name: str) -> dict:
-    if name == "writer_sweep":
-        return W.writer_sweep(H=16)
+def make_workload(name: str, heads: int = 16, layout: str = "raw512") -> dict:
+    if name == "writer_sweep":   # decode over freshly written rows: --heads, --layout
+        if layout not in ("raw512", "scaled528"):
+            raise SystemExit("writer_sweep takes --layout raw512 or scaled528")
+        return W.writer_sweep(H=heads, layout=layout)
     return W.make(name)
 
 
@@ -113,7 +116,7 @@ def run_gather(args) -> dict:
 
     from sparse_mla_attention_page_gb300 import binding
     dev = torch.device("cuda", 0)
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.heads, args.layout)
     T, K, layout = w["T"], w["K"], w["layout"]
     R = 512 if layout == "raw512" else 528
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
@@ -287,7 +290,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.heads, args.layout)
     T, H, K = w["T"], w["H"], w["K"]
     layout = w["layout"]
     prefill = w["name"].startswith("prefill_q8")
@@ -534,7 +537,7 @@ def cpu_baseline(w: dict, seconds: float) -> dict:
 def run_reference(args, rank: int):
     if rank != 0:
         return None
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.heads, args.layout)
     cores = len(os.sched_getaffinity(0))
     pool, q8, qs = oracle_setup(w)
     x_new, slots = step_rows(w)
