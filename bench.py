@@ -68,6 +68,9 @@ def parse_args():
     p.add_argument("--layout", choices=["raw512", "scaled528", "rope656"], default="raw512",
                    help="row layout of --op kv_write and of --workload writer_sweep (raw512, scaled528)")
     p.add_argument("--heads", type=int, default=16, help="head count of --workload writer_sweep")
+    p.add_argument("--warm", action="store_true",
+                   help="informational: no L2 flush between steps (inputs may stay in L2); "
+                        "the default run flushes before every step")
     return p.parse_args()
 
 
@@ -321,6 +324,10 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def flush():
+        if not args.warm:
+            flush_buf.zero_()
+
     def step_write():
         write(x_new, slots, pool)
         if prefill:
@@ -338,7 +345,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     launches_per_step = 1 + (1 if prefill else 0) + 1 + (1 if ws is not None else 0)
 
     for _ in range(args.warmup):
-        flush_buf.zero_()
+        flush()
         step_write()
         step_attn()
     torch.cuda.synchronize(dev)
@@ -358,7 +365,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
     for i in range(args.steps):
-        flush_buf.zero_()
+        flush()
         ev[i][0].record(stream)
         step_write()
         step_attn()
@@ -370,7 +377,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     # L2 flush before every call, the inputs of the last step
     ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush_buf.zero_()
+        flush()
         ev_a[i][0].record(stream)
         step_attn()
         ev_a[i][1].record(stream)
@@ -427,7 +434,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
     for i in range(n_e2e + 3):
-        flush_buf.zero_()
+        flush()
         if i >= 3:
             e2e_ev[i - 3][0].record(stream)
         d_in.copy_(h_in, non_blocking=True)
@@ -467,7 +474,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
                    "pool_rows": w["pool_rows"], "page_size": w["page_size"],
                    "valid_entries": W.valid_entry_count(w["topk"]),
                    "step": ("quantize_q8 + " if prefill else "") + f"kv_write_{layout[:3]} of {T} new rows + sparse attention",
-                   "l2": f"flushed before every step ({flush_buf.numel() >> 20} MiB write)",
+                   "l2": ("not flushed (warm; informational)" if args.warm
+                          else f"flushed before every step ({flush_buf.numel() >> 20} MiB write)"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
