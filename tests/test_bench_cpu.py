@@ -1,0 +1,65 @@
+"""CPU checks of bench.py: the byte and flop counts behind the roofline, its
+defaults, and the JSON line of the reference arm (the oracle, run on the host)."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from sparse_mla_attention_page_gb300 import workloads as W  # noqa: E402
+
+
+def test_algorithmic_bytes_decode():
+    """Each valid entry's 512-byte row once, BF16 Q and O, int32 top-k, FP32 LSE."""
+    w = W.tiny_decode_raw512()
+    T, H, K = w["T"], w["H"], w["K"]
+    valid = int((w["topk"] >= 0).sum())
+    assert valid == T * (K - 16)                  # the tiny case masks a 16-entry tail
+    expect = valid * 512 + T * H * 512 * 2 + T * K * 4 + T * H * 512 * 2 + T * H * 4
+    assert bench.algorithmic_bytes(w) == expect
+    assert bench.attn_flops(w) == 4 * H * 512 * valid
+
+
+def test_algorithmic_bytes_prefill_and_rope():
+    """Q8 prefill: one-byte queries plus an FP32 scale per (token, head); 656-byte rows:
+    576-wide BF16 queries and keys, values over the 512 latent dims."""
+    w = W.prefill_q8_raw512(T=8, context=256, pool_rows=512)
+    T, H, K = w["T"], w["H"], w["K"]
+    valid = int((w["topk"] >= 0).sum())
+    assert valid == sum(min(K, 256 + t + 1) for t in range(T))
+    expect = valid * 512 + T * H * 512 + T * H * 4 + T * K * 4 + T * H * 512 * 2 + T * H * 4
+    assert bench.algorithmic_bytes(w) == expect
+    r = W.decode_rope656(T=2, K=256, pool_rows=4096)
+    v = int((r["topk"] >= 0).sum())
+    assert bench.algorithmic_bytes(r) == (v * 656 + r["T"] * r["H"] * 576 * 2 + r["T"] * r["K"] * 4
+                                          + r["T"] * r["H"] * 512 * 2 + r["T"] * r["H"] * 4)
+    assert bench.attn_flops(r) == 2 * r["H"] * (576 + 512) * v
+
+
+def test_defaults(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse_args()
+    assert (a.gpus, a.impl, a.workload, a.op) == (1, "ours", "decode_raw512", "attention")
+    assert a.warmup >= 3 and a.steps >= 1 and not a.warm
+
+
+def test_reference_arm_line():
+    """The reference arm times the oracle on the host cores and prints one JSON line
+    with the metric, the impl tag, a cpu_baseline and an e2e with no copies."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny_decode_raw512", "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and np.isfinite(d["value"])
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny_decode_raw512" and d["higher_is_better"] is True
