@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -214,10 +215,16 @@ def measured_peaks() -> dict:
 
 
 def kernel_source_sha() -> str:
+    """Hash of the attention kernels' code with comments and blank lines removed, so
+    that recorded ncu counters stay valid across comment-only edits."""
     h = hashlib.sha256()
     for rel in ATTN_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        code = "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

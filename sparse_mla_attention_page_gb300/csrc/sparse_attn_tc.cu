@@ -28,16 +28,19 @@
 //              tensor memory, issued in whatever order their inputs become
 //              ready (one MMA of K=32 occupies the tensor pipe for the same
 //              ~64 cycles for any N up to 128, so the pipe must never wait on
-//              one queue while the other is ready).  The same shared-memory tile is
-//              the K-major A operand of the first and the MN-major A operand
+//              one queue while the other is ready).  The same shared-memory
+//              tile is the K-major A operand of the first and the MN-major A operand
 //              of the second (V = K: one absorbed NoPE latent row).  Over
 //              656-byte rows, four kind::f16 MMAs per tile add the BF16 RoPE
 //              scores K_rope Q_rope^T in extra score columns.
 //   softmax    8 warps, two per TMEM lane quarter, each thread one tile row
-//              (= TMEM lane) and half of the heads: combine the
-//              score columns, mask, reduce the tile max per head across the
-//              128 rows, keep a lazy running max (O in TMEM is rescaled only
-//              when the max grows by more than 2^8), form p = 2^(s - m),
+//              (= TMEM lane) and half of the heads: combine the score
+//              columns, mask, keep a lazy running max (one barrier with an
+//              OR reduction asks whether any row exceeds its head's running
+//              max by more than 2^8; only then are the per-head tile maxima
+//              across the 128 rows formed and O in TMEM rescaled; 528-byte
+//              rows, which also track the group-scale exponents, form them
+//              every tile), form p = 2^(s - m),
 //              accumulate the denominators, write P as an FP8 operand, build
 //              each segment's query operand in shared memory (loads issued a
 //              tile ahead), and at the end of a segment normalise O and store
