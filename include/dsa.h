@@ -84,11 +84,19 @@ enum {
 /* Human-readable name of a status code (static string). */
 const char* dsa_status_string(int status);
 
-/* Bytes of one physical KV row: 512 or 528 ("exported buffer lengths",
+/* Bytes of one physical KV row: 512, 528 or 656 ("exported buffer lengths",
  * [P1 Speed Tests and Profiling]); 0 for an unknown layout. */
 size_t dsa_kv_row_bytes(int layout);
 
 /* ------------------------------------------------------------- KV writers */
+
+/* Stream ordering of the writers: each writer kernel releases its programmatic
+ * dependents as it starts (griddepcontrol.launch_dependents).  A kernel that
+ * the caller launches next on the same stream with programmatic stream
+ * serialization may therefore begin while the writer still runs, and must
+ * execute griddepcontrol.wait before it reads the pool (the attention entry
+ * points below do).  Kernels launched without that attribute, copies and
+ * events are ordered after the writer as usual. */
 
 /* Fused cast + paged scatter of new latent rows into a raw512 pool
  * [P1 Motivation, Modifications: the fused cast/paged writer, selected by
@@ -157,7 +165,7 @@ size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
  *                   DSA_ERR_ROW_WIDTH); over 656-byte rows the query is
  *                   [T, H, 576] (latent dims, then the 64 RoPE dims), the
  *                   scores use all 576 dims and O the 512 latent dims.
- *   pool_dev        [pool_rows, 512 or 528] bytes, 16-byte aligned.
+ *   pool_dev        [pool_rows, 512, 528 or 656] bytes, 16-byte aligned.
  *   page_table_dev  [B, max_pages] int32 physical page ids, or NULL.
  *   token_seq_dev   [T] int32 sequence id per token, or NULL (all sequence 0).
  *   topk_dev        [T, K] int32, K a positive multiple of 128.
@@ -166,7 +174,13 @@ size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
  *   workspace_dev   ws_bytes >= dsa_sparse_attn_workspace_bytes(T, H, K).
  *   err_flag_dev    nullable int32 error bits.
  * H must be one of 8, 16, 32, 64, 128 (8 or 16 over 656-byte rows).
- * T == 0 is a no-op. */
+ * T == 0 is a no-op.
+ * Launch: the attention kernel is launched with programmatic stream
+ * serialization; it may start its set-up while the previous kernel on the
+ * stream runs (if that kernel released its dependents early, as the writers
+ * do) and executes griddepcontrol.wait before it reads or writes any global
+ * memory, so the stream order of all inputs and outputs is kept.  The
+ * split-unit merge that follows it is launched the same way. */
 int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D,
                            const void* pool_dev, int64_t pool_rows, int layout, int kv_row_dim,
                            const int32_t* page_table_dev, int B, int max_pages, int page_size,
