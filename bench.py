@@ -206,6 +206,17 @@ def run_kv_write(args) -> dict:
                          "frac": round(achieved / peak, 4), "algorithmic_bytes_per_call": abytes}}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (x itself with no process group): a job is
+    as slow as its slowest rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -394,11 +405,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     sampler.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     attn_ms = [e[0].elapsed_time(e[1]) for e in ev_a]
-    total_ms = float(sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
 
     # end to end through the public API: the step's inputs from one pinned host
     # buffer (one H2D copy), the results back in one D2H copy
@@ -457,11 +464,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
         if i >= 3:
             e2e_ev[i - 3][1].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = float(sum(e[0].elapsed_time(e[1]) for e in e2e_ev))
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(float(sum(e[0].elapsed_time(e[1]) for e in e2e_ev)), dist, dev)
 
     if rank != 0:
         return None

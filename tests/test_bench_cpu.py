@@ -1,11 +1,15 @@
 """CPU checks of bench.py: the byte and flop counts behind the roofline, its
-defaults, and the JSON line of the reference arm (the oracle, run on the host)."""
+defaults, the JSON line of the reference arm (the oracle, run on the host), and
+the multi-rank path on two gloo ranks (max-over-ranks timing, rank 0 alone
+printing)."""
 import json
 import os
+import socket
 import subprocess
 import sys
 
 import numpy as np
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -63,3 +67,43 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny_decode_raw512" and d["higher_is_better"] is True
+
+
+def _free_port() -> int:
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, out_dir: str):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    v = bench.max_over_ranks(1.5 + rank, dist, "cpu")
+    with open(os.path.join(out_dir, f"rank{rank}"), "w") as f:
+        f.write(repr(v))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks(tmp_path):
+    """The timed region of a multi-rank run is the slowest rank's: every rank gets
+    the maximum (two gloo ranks on the CPU)."""
+    torch.multiprocessing.spawn(_rank_main, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    assert [float((tmp_path / f"rank{r}").read_text()) for r in range(2)] == [2.5, 2.5]
+    assert bench.max_over_ranks(3.0, None, "cpu") == 3.0
+
+
+def test_reference_arm_two_ranks():
+    """Launched as the driver launches N > 1 (torchrun, one process per rank), the
+    reference arm runs on rank 0 alone: one JSON line, every rank exits 0."""
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                          "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+                          os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny_decode_raw512",
+                          "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["impl"] == "reference"
