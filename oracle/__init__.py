@@ -55,6 +55,8 @@ def load(path: str):
     L.oracle_quantize_q8.restype = None
     L.oracle_quantize_q8.argtypes = [c.c_void_p, c.c_int64, c.c_int, c.c_void_p, c.c_void_p]
     L.oracle_sparse_attn.restype = c.c_int
+    L.oracle_gather_rows.restype = c.c_int64
+    L.oracle_gather_rows.argtypes = [c.c_int64, c.c_int64]
     L.oracle_gather_dequant.restype = c.c_int
     L.oracle_gather_dequant.argtypes = [c.c_void_p, c.c_int64, c.c_int, c.c_void_p, c.c_int, c.c_int, c.c_int,
                                         c.c_void_p, c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_void_p]
@@ -201,24 +203,32 @@ def sparse_attn(pool: np.ndarray, layout: str, topk: np.ndarray, sm_scale: float
     return O, LSE, int(err)
 
 
+def gather_rows(pool_rows: int, n_selected: int) -> int:
+    """Rows of the reader's BF16 workspace: min(pool_rows, selected entries)."""
+    return int(lib().oracle_gather_rows(int(pool_rows), int(n_selected)))
+
+
 def gather_dequant(pool: np.ndarray, layout: str, topk: np.ndarray, *,
                    page_table: np.ndarray | None = None, page_size: int = 64,
                    token_seq: np.ndarray | None = None):
-    """BF16 rows (uint16 [T*K, 512]; masked slots stay 0 here), remapped
-    indices (int32 [T, K]) and error bits, as the reader defines them."""
+    """The reader's BF16 workspace (uint16 [gather_rows(pool_rows, T*K), W],
+    W = 512, or 576 for 656-byte rows; rows it leaves alone stay 0 here),
+    remapped indices (int32 [T, K]) and error bits.  With T*K < pool_rows
+    the workspace holds the selected rows and idx_out the entry numbers;
+    otherwise it holds the whole pool and idx_out the physical rows."""
     topk = np.ascontiguousarray(topk, dtype=np.int32)
     T, K = topk.shape
     pool = np.ascontiguousarray(pool, dtype=np.uint8)
-    assert layout in ("raw512", "scaled528") and pool.shape[1] == row_bytes(layout)
+    assert pool.shape[1] == row_bytes(layout)
     if page_table is not None:
         pt = np.ascontiguousarray(page_table, dtype=np.int32)
         B, max_pages = pt.shape
     else:
         pt, B, max_pages = None, 1, 0
     ts = None if token_seq is None else np.ascontiguousarray(token_seq, dtype=np.int32)
-    out = np.zeros((T * K, 512), dtype=np.uint16)
+    out = np.zeros((gather_rows(pool.shape[0], T * K), key_width(layout)), dtype=np.uint16)
     idx = np.zeros((T, K), dtype=np.int32)
-    err = lib().oracle_gather_dequant(_ptr(pool), pool.shape[0], 0 if layout == "raw512" else 1,
+    err = lib().oracle_gather_dequant(_ptr(pool), pool.shape[0], LAYOUT_CODES[layout],
                                       _ptr(pt), B, max_pages, page_size, _ptr(ts), _ptr(topk), T, K,
                                       _ptr(out), _ptr(idx))
     return out, idx, int(err)

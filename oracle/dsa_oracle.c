@@ -33,9 +33,8 @@
  * gives O = 0, LSE = -inf; an index outside
  * the pool or the page table is masked and reported through an error bit;
  * a zero group gets scale 0 and zero bytes; an input that saturates maps to
- * +-448; a negative input that rounds to zero keeps its sign (0x80).
- *
- * Parity unpinned: NaN inputs (the sign and payload of an encoded NaN).
+ * +-448; a negative input that rounds to zero keeps its sign (0x80); a NaN
+ * input (any payload) encodes as the FN NaN code 0x7F with its sign bit.
  *
  * Arithmetic: float64 throughout, except where the definition itself fixes
  * FP32 (the writer's scale amax/448 and the division x/s, which the format
@@ -432,16 +431,50 @@ static uint16_t f32_to_bf16_rne(float f) {
   return (uint16_t)(u >> 16);
 }
 
-/* The rows a top-k list selects, dequantised to BF16, in one padded buffer
- * ("[DSA] Support group-scaled FP8 NoPE KV reads for CUDA TileLang",
- * Modifications: the gather/cast reader that feeds BF16 consumers; pull 44217,
- * review thread: the paged gather with -1 padding).  For entry j of token t,
- * slot e = t*K + j:
- *   out[e][d] = bf16_rne( fp32( e4m3(b_d) * s_g ) )  (raw rows: s = 1, exact),
- *   idx_out[e] = e for a valid entry, -1 for a masked one (its out row is
- *   left as it is).  Rows resolve as in the attention (same error bits).
- * The FP32 product is formed once (the exact product fits a double; the cast
- * rounds it to nearest FP32), then rounded to BF16. */
+/* The reader's BF16 workspace ("[DSA] Support group-scaled FP8 NoPE KV reads
+ * for CUDA TileLang", Modifications, second bullet): when the top-k lists hold
+ * fewer entries than the pool has physical rows, only the selected rows are
+ * dequantised, one workspace row per top-k entry; otherwise the whole pool is
+ * dequantised, one workspace row per physical row.  Either way the workspace
+ * has min(pool_rows, T*K) rows, which bounds it at min(physical rows,
+ * selected entries) * 1024 bytes for 512-wide BF16 rows.  The count is fixed
+ * by the shapes alone (no data-dependent unique step, so nothing is read back
+ * from the device to size it). */
+int64_t oracle_gather_rows(int64_t pool_rows, int64_t n_selected) {
+  return n_selected < pool_rows ? n_selected : pool_rows;
+}
+
+/* One physical row dequantised to BF16: the 512 latent dims
+ * bf16_rne(fp32(e4m3(b_d) * s_g)) (raw rows: s = 1, exact), then for
+ * 656-byte rows the 64 RoPE dims as stored (BF16 bits).  The FP32 product is
+ * formed once (the exact product fits a double; the cast rounds it to the
+ * nearest FP32), then rounded to BF16. */
+static void dequant_row_bf16(const uint8_t* r, int layout, uint16_t* out) {
+  for (int d = 0; d < ORACLE_D; ++d) {
+    const int g = d / ORACLE_GROUP;                 /* the 128-dim group of d */
+    double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * g);
+    float v = (float)(oracle_e4m3_decode(r[d]) * s);
+    out[d] = f32_to_bf16_rne(v);
+  }
+  if (layout == 2)
+    for (int j = 0; j < ORACLE_ROPE; ++j)
+      out[ORACLE_D + j] = (uint16_t)(((unsigned)r[528 + 2 * j + 1] << 8) | r[528 + 2 * j]);
+}
+
+/* The gather/dequantise reader that feeds BF16 consumers ("[DSA] Support
+ * group-scaled FP8 NoPE KV reads for CUDA TileLang", Modifications: the full
+ * and paged readers, the selected-row workspace with remapped indices and
+ * kept masks; pull 44217, review thread: the paged gather with -1 padding).
+ * Rows resolve as in the attention (same error bits).  out has
+ * oracle_gather_rows(pool_rows, T*K) rows of W = 512 values (576 for
+ * 656-byte rows, the RoPE dims appended).  For entry j of token t, e = t*K + j:
+ *  - selected branch (T*K < pool_rows): out[e] = the entry's dequantised row
+ *    and idx_out[e] = e;
+ *  - full-pool branch (T*K >= pool_rows): out[r] = dequantised physical row r
+ *    for every r, and idx_out[e] = the entry's physical row;
+ *  - a masked entry gets idx_out[e] = -1 (in the selected branch its out row
+ *    is left as it is).
+ * So out[idx_out[e]] is entry e's row in both branches. */
 int oracle_gather_dequant(const uint8_t* pool, int64_t pool_rows, int layout,
                           const int32_t* page_table, int B, int max_pages, int page_size,
                           const int32_t* token_seq, const int32_t* topk, int T, int K,
@@ -452,19 +485,23 @@ int oracle_gather_dequant(const uint8_t* pool, int64_t pool_rows, int layout,
   J.page_table = page_table; J.B = B; J.max_pages = max_pages; J.page_size = page_size;
   J.token_seq = token_seq;
   int err = 0;
-  const int64_t R = layout == 0 ? 512 : 528;
+  const int64_t R = layout == 0 ? 512 : layout == 1 ? 528 : 656;
+  const int W = layout == 2 ? ORACLE_D + ORACLE_ROPE : ORACLE_D;
+  const int64_t n_sel = (int64_t)T * K;
+  const int full_pool = !(n_sel < pool_rows);
+  if (full_pool)
+    for (int64_t r = 0; r < pool_rows; ++r) dequant_row_bf16(pool + r * R, layout, out + r * W);
   for (int t = 0; t < T; ++t) {
     for (int j = 0; j < K; ++j) {
       const int64_t e = (int64_t)t * K + j;
       const int64_t row = resolve_row(&J, t, topk[e], &err);
-      idx_out[e] = row < 0 ? -1 : (int32_t)e;
-      if (row < 0) continue;
-      const uint8_t* r = pool + row * R;
-      for (int d = 0; d < ORACLE_D; ++d) {
-        const int g = d / ORACLE_GROUP;                 /* the 128-dim group of d */
-        double s = layout == 0 ? 1.0 : (double)le_f32(r + 512 + 4 * g);
-        float v = (float)(oracle_e4m3_decode(r[d]) * s);
-        out[e * ORACLE_D + d] = f32_to_bf16_rne(v);
+      if (row < 0) {
+        idx_out[e] = -1;
+      } else if (full_pool) {
+        idx_out[e] = (int32_t)row;
+      } else {
+        idx_out[e] = (int32_t)e;
+        dequant_row_bf16(pool + row * R, layout, out + e * W);
       }
     }
   }

@@ -97,6 +97,23 @@ def pin_encode_roundtrip():
 
 # ------------------------------------------------------------------- writers
 
+def pin_encode_nan():
+    """NaN inputs: every FP32 NaN encoding (quiet and signalling payloads, both
+    signs) and every BF16 NaN bit pattern encodes as PyTorch's float8_e4m3fn
+    cast does: the FN NaN code 0x7F with the input's sign bit."""
+    f32 = np.array([0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF800001, 0x7FFFFFFF, 0xFFFFFFFF, 0x7FA00000],
+                   dtype=np.uint32).view(np.float32)
+    bf = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    bf = bf[((bf & 0x7F80) == 0x7F80) & ((bf & 0x7F) != 0)]
+    x = np.concatenate([f32, W.bf16_bits_to_f32(bf)])
+    assert np.isnan(x).all() and x.size == 7 + 2 * 127
+    want = _torch_encode(x)
+    for brute in (False, True):
+        got = oracle.e4m3_encode_array(x, bruteforce=brute)
+        np.testing.assert_array_equal(got, want)
+    assert set(want.tolist()) == {0x7F, 0xFF}
+
+
 def _bf16_row(values: np.ndarray) -> np.ndarray:
     bits = W.f32_to_bf16_bits(values.astype(np.float32))
     assert np.array_equal(W.bf16_bits_to_f32(bits), values.astype(np.float32)), "fixture not BF16-exact"
@@ -391,36 +408,98 @@ def pin_wrong_index_is_detected():
     assert (diff > 0).any()
 
 
-def pin_gather_dequant_torch():
-    """The reader's BF16 rows are PyTorch's own FP8 decode (raw rows, exact in
-    BF16) and PyTorch's FP32 product with the group scale cast to BF16 (scaled
-    rows); its remapped indices are the slot numbers, -1 where masked; an
-    entry outside the page table is masked with the same error bit as the
-    attention."""
+def _torch_rows_bf16(pool: np.ndarray, layout: str, rows: np.ndarray) -> np.ndarray:
+    """BF16 bits of physical rows dequantised by PyTorch: its own FP8 decode
+    (raw rows, exact in BF16), or its FP32 product with the group scale cast
+    to BF16; 656-byte rows append their stored RoPE bits."""
+    rows = np.asarray(rows, dtype=np.int64)
+    r = torch.from_numpy(np.ascontiguousarray(pool[rows, :512])).view(torch.float8_e4m3fn)
+    if layout == "raw512":
+        v = r.to(torch.bfloat16)
+    else:
+        sc = torch.from_numpy(np.ascontiguousarray(pool[rows, 512:528]).view("<f4").copy())
+        v = (r.to(torch.float32) * sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
+    out = v.view(torch.int16).numpy().view(np.uint16)
+    if layout == "rope656":
+        out = np.concatenate([out, np.ascontiguousarray(pool[rows, 528:656]).view("<u2")], axis=1)
+    return out
+
+
+def _tiny_rope(seed: int, T: int, K: int, pool_rows: int):
+    w = W.decode_rope656(seed=seed, T=T, H=2, K=K, pool_rows=pool_rows)
+    w["token_seq"] = None
+    return w, oracle.fill_pool(w)
+
+
+def pin_gather_selected_branch():
+    """Fewer top-k entries than pool rows: the workspace has one row per entry
+    (T*K rows), each the PyTorch dequantisation of the entry's physical row;
+    the remapped index of an entry is its entry number, -1 where masked; an
+    entry outside the page table is masked with the attention's error bit."""
     for layout, seed, seqs in (("raw512", 81, 1), ("scaled528", 82, 2)):
         w, pool = _tiny(layout, seed, T=4, K=128, seqs=seqs)
         topk = w["topk"].copy()
+        T, K = topk.shape
+        assert T * K < w["pool_rows"]
         out, idx, err = oracle.gather_dequant(pool, layout, topk, page_table=w["page_table"],
                                               page_size=64, token_seq=w["token_seq"])
-        assert err == 0
-        T, K = topk.shape
+        assert err == 0 and out.shape == (T * K, 512)
         want_idx = np.where(topk >= 0, np.arange(T * K, dtype=np.int32).reshape(T, K), -1)
         np.testing.assert_array_equal(idx, want_idx)
         e = np.nonzero(topk.reshape(-1) >= 0)[0]
         rows = np.array([_phys(w["page_table"], w["token_seq"], int(i) // K, int(topk.reshape(-1)[i]))
                          for i in e])
-        r = torch.from_numpy(np.ascontiguousarray(pool[rows, :512])).view(torch.float8_e4m3fn)
-        if layout == "raw512":
-            want = r.to(torch.bfloat16)
-        else:
-            sc = torch.from_numpy(np.ascontiguousarray(pool[rows, 512:]).view("<f4").copy())
-            want = (r.to(torch.float32) * sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
-        np.testing.assert_array_equal(out[e], want.view(torch.int16).numpy().view(np.uint16))
+        np.testing.assert_array_equal(out[e], _torch_rows_bf16(pool, layout, rows))
+        masked = np.nonzero(topk.reshape(-1) < 0)[0]
+        assert masked.size and not out[masked].any()          # masked rows are not written
     bad = topk.copy()
     bad[0, 0] = w["page_table"].shape[1] * 64 + 1          # beyond the page table's width
     _, idx2, err2 = oracle.gather_dequant(pool, "scaled528", bad, page_table=w["page_table"],
                                           page_size=64, token_seq=w["token_seq"])
     assert err2 == oracle.ERR_INDEX_RANGE and idx2[0, 0] == -1
+
+
+def pin_gather_full_pool_branch():
+    """As many top-k entries as pool rows, or more: the workspace is the whole
+    pool dequantised by PyTorch (pool_rows rows), and each entry's remapped
+    index is its physical row (page table applied), -1 where masked.  The
+    boundary T*K == pool_rows already takes this branch."""
+    for layout, seed, T, K in (("raw512", 83, 4, 128), ("scaled528", 84, 6, 128)):
+        w, pool = _tiny(layout, seed, T=T, K=K, pool_rows=512, seqs=2)
+        topk = w["topk"]
+        assert T * K >= w["pool_rows"]
+        out, idx, err = oracle.gather_dequant(pool, layout, topk, page_table=w["page_table"],
+                                              page_size=64, token_seq=w["token_seq"])
+        assert err == 0 and out.shape == (w["pool_rows"], 512)
+        np.testing.assert_array_equal(out, _torch_rows_bf16(pool, layout, np.arange(w["pool_rows"])))
+        want = np.array([[_phys(w["page_table"], w["token_seq"], t, int(i)) if i >= 0 else -1
+                          for i in topk[t]] for t in range(T)], dtype=np.int32)
+        np.testing.assert_array_equal(idx, want)
+
+
+def pin_gather_rows_bound():
+    """The workspace row count is min(pool rows, selected entries): its BF16
+    payload is bounded by min(physical_tokens, selected_entries) * 1024 bytes."""
+    for pool_rows, n in ((1024, 512), (1024, 1023), (1024, 1024), (1024, 1025), (131072, 262144),
+                         (16384, 8388608), (4096, 0)):
+        assert oracle.gather_rows(pool_rows, n) == min(pool_rows, n), (pool_rows, n)
+
+
+def pin_gather_rope656():
+    """656-byte rows in both branches: 576-wide BF16 workspace rows, the
+    latent dims dequantised as for 528-byte rows and the RoPE dims copied."""
+    for T, K, pool_rows in ((2, 128, 1024), (4, 256, 1024)):
+        w, pool = _tiny_rope(85 + T, T, K, pool_rows)
+        topk = w["topk"]
+        out, idx, err = oracle.gather_dequant(pool, "rope656", topk, page_table=w["page_table"], page_size=64)
+        assert err == 0 and out.shape == (min(pool_rows, T * K), 576)
+        for t in range(T):
+            for j in range(K):
+                if topk[t, j] < 0:
+                    assert idx[t, j] == -1
+                    continue
+                row = _phys(w["page_table"], None, t, int(topk[t, j]))
+                np.testing.assert_array_equal(out[idx[t, j]], _torch_rows_bf16(pool, "rope656", [row])[0])
 
 
 def pin_rope656():
@@ -457,5 +536,6 @@ ALL_PINS = [
     pin_encode_roundtrip, pin_scaled_worked_example, pin_raw_writer_torch,
     pin_scaled_writer_invariants, pin_attn_sdpa, pin_attn_closed_forms, pin_attn_invariances,
     pin_q8_matches_bf16_decode, pin_q8_quantiser, pin_error_bits, pin_wrong_index_is_detected,
-    pin_gather_dequant_torch, pin_rope656,
+    pin_gather_selected_branch, pin_gather_full_pool_branch,
+    pin_gather_rows_bound, pin_gather_rope656, pin_rope656, pin_encode_nan,
 ]

@@ -47,7 +47,18 @@ MUTANTS = {
     "rope_read_byte_order": ("(uint16_t)(r[528 + 2 * j] | (r[528 + 2 * j + 1] << 8))",
                              "(uint16_t)(r[528 + 2 * j + 1] | (r[528 + 2 * j] << 8))"),
     "rope_write_byte_order": ("row[528 + 2 * j] = (uint8_t)(b & 0xFF);", "row[528 + 2 * j] = (uint8_t)(b >> 8);"),
-    "reader_index_not_remapped": ("idx_out[e] = row < 0 ? -1 : (int32_t)e;", "idx_out[e] = row < 0 ? -1 : topk[e];"),
+    "reader_index_not_remapped": ("idx_out[e] = (int32_t)e;\n        dequant_row_bf16",
+                                  "idx_out[e] = topk[e];\n        dequant_row_bf16"),
+    "reader_branch_boundary": ("const int full_pool = !(n_sel < pool_rows);", "const int full_pool = !(n_sel <= pool_rows);"),
+    "reader_full_pool_keeps_entry": ("idx_out[e] = (int32_t)row;", "idx_out[e] = (int32_t)e;"),
+    "reader_full_pool_short": ("for (int64_t r = 0; r < pool_rows; ++r) dequant_row_bf16",
+                               "for (int64_t r = 0; r + 1 < pool_rows; ++r) dequant_row_bf16"),
+    "reader_rows_bound_max": ("return n_selected < pool_rows ? n_selected : pool_rows;",
+                              "return n_selected < pool_rows ? pool_rows : n_selected;"),
+    "reader_rope_dropped": ("out[ORACLE_D + j] = (uint16_t)(((unsigned)r[528 + 2 * j + 1] << 8) | r[528 + 2 * j]);",
+                            "out[ORACLE_D + j] = 0;"),
+    "nan_sign_dropped": ("pthread_once(&g_table_once, build_table);\n  uint8_t sign = signbit(x) ? 0x80 : 0x00;\n  if (isnan(x)) return (uint8_t)(sign | 0x7F);",
+                         "pthread_once(&g_table_once, build_table);\n  uint8_t sign = signbit(x) ? 0x80 : 0x00;\n  if (isnan(x)) return (uint8_t)0x7F;"),
 }
 
 
