@@ -164,7 +164,10 @@ int64_t oracle_kv_write_raw(const uint16_t* x, int64_t n_rows, const int64_t* sl
 }
 
 /* One group of 128 values: s = amax/448 in FP32; q = e4m3(x/s) with the FP32
- * quotient; amax == 0 gives s = 0 and zero bytes. */
+ * quotient; amax == 0 gives s = 0 and zero bytes.  A NaN value encodes as
+ * NaN with its own sign (the sign a division gives a NaN is left open by
+ * IEEE 754, so it is not taken from the quotient); amax is over the values
+ * that are not NaN. */
 static float scaled_group(const float* v, uint8_t* q) {
   float amax = 0.0f;
   for (int i = 0; i < ORACLE_GROUP; ++i) {
@@ -177,8 +180,7 @@ static float scaled_group(const float* v, uint8_t* q) {
   }
   float s = amax / 448.0f;
   for (int i = 0; i < ORACLE_GROUP; ++i) {
-    float r = v[i] / s;
-    q[i] = oracle_e4m3_encode(r);
+    q[i] = isnan(v[i]) ? oracle_e4m3_encode(v[i]) : oracle_e4m3_encode(v[i] / s);
   }
   return s;
 }
@@ -233,7 +235,9 @@ int64_t oracle_kv_write_rope656(const uint16_t* x, int64_t n_rows, const int64_t
 }
 
 /* FP8 query quantiser: per (token, head) vector of d values,
- * scale = amax/448 (FP32), q8 = e4m3(q/scale); amax == 0 gives scale 0, zeros. */
+ * scale = amax/448 (FP32), q8 = e4m3(q/scale); amax == 0 gives scale 0, zeros.
+ * NaN values as in the group-scaled writer: NaN with their own sign, left out
+ * of amax. */
 void oracle_quantize_q8(const uint16_t* q, int64_t n_vec, int d, uint8_t* q8, float* scale) {
   float* v = (float*)malloc(sizeof(float) * (size_t)d);
   for (int64_t i = 0; i < n_vec; ++i) {
@@ -249,7 +253,8 @@ void oracle_quantize_q8(const uint16_t* q, int64_t n_vec, int d, uint8_t* q8, fl
       continue;
     }
     float s = amax / 448.0f;
-    for (int j = 0; j < d; ++j) q8[i * d + j] = oracle_e4m3_encode(v[j] / s);
+    for (int j = 0; j < d; ++j)
+      q8[i * d + j] = isnan(v[j]) ? oracle_e4m3_encode(v[j]) : oracle_e4m3_encode(v[j] / s);
     scale[i] = s;
   }
   free(v);

@@ -114,6 +114,31 @@ def pin_encode_nan():
     assert set(want.tolist()) == {0x7F, 0xFF}
 
 
+def pin_nan_in_scaled_writer_and_quantiser():
+    """NaN elements of a group-scaled row or of a query vector: the scale is
+    taken over the other values (NumPy's nanmax / 448 in FP32) and the NaN
+    encodes as 0x7F with its own sign, whatever sign a division would give."""
+    rng = np.random.default_rng(17)
+    xf = rng.standard_normal((4, 512)).astype(np.float32)
+    nan_pos = [(0, 3, 0), (1, 200, 1), (2, 511, 0), (3, 0, 1), (3, 130, 1)]   # (row, dim, negative)
+    x = W.f32_to_bf16_bits(xf)
+    for r, d, neg in nan_pos:
+        x[r, d] = 0xFFC0 if neg else 0x7FC0
+    xv = W.bf16_bits_to_f32(x)
+    pool = oracle.new_pool(4, "scaled528")
+    oracle.kv_write("scaled528", x, np.arange(4), pool)
+    sc = pool[:, 512:].copy().view("<f4")
+    amax = np.nanmax(np.abs(xv.reshape(4, 4, 128)), axis=2)
+    np.testing.assert_array_equal(sc, (amax / np.float32(448)).astype(np.float32))
+    q8, qs = oracle.quantize_q8(x.reshape(4, 1, 512))
+    np.testing.assert_array_equal(qs[:, 0], (np.nanmax(np.abs(xv), axis=1) / np.float32(448)).astype(np.float32))
+    for r, d, neg in nan_pos:
+        assert pool[r, d] == (0xFF if neg else 0x7F), (r, d, pool[r, d])
+        assert q8[r, 0, d] == (0xFF if neg else 0x7F), (r, d, q8[r, 0, d])
+    finite = ~np.isnan(xv)
+    assert not np.isin(pool[:, :512][finite], [0x7F, 0xFF]).any()
+
+
 def _bf16_row(values: np.ndarray) -> np.ndarray:
     bits = W.f32_to_bf16_bits(values.astype(np.float32))
     assert np.array_equal(W.bf16_bits_to_f32(bits), values.astype(np.float32)), "fixture not BF16-exact"
@@ -538,4 +563,5 @@ ALL_PINS = [
     pin_q8_matches_bf16_decode, pin_q8_quantiser, pin_error_bits, pin_wrong_index_is_detected,
     pin_gather_selected_branch, pin_gather_full_pool_branch,
     pin_gather_rows_bound, pin_gather_rope656, pin_rope656, pin_encode_nan,
+    pin_nan_in_scaled_writer_and_quantiser,
 ]

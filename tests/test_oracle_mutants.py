@@ -36,8 +36,8 @@ MUTANTS = {
     "softmax_sign": ("l += exp(s[j] - m);", "l += exp(m - s[j]);"),
     "values_not_rows": ("o[d] += p * k[d];", "o[d] += p * q[d];"),
     "q8_scale_dropped": ("q[d] = oracle_e4m3_decode(q8[d]) * sc;", "q[d] = oracle_e4m3_decode(q8[d]);"),
-    "q8_divisor": ("    float s = amax / 448.0f;\n    for (int j = 0; j < d; ++j) q8",
-                   "    float s = amax / 512.0f;\n    for (int j = 0; j < d; ++j) q8"),
+    "q8_divisor": ("    float s = amax / 448.0f;\n    for (int j = 0; j < d; ++j)\n      q8",
+                   "    float s = amax / 512.0f;\n    for (int j = 0; j < d; ++j)\n      q8"),
     "index_range_unchecked": ("if (page >= J->max_pages) { *err |= ORACLE_ERR_INDEX_RANGE; return -1; }",
                               "if (page >= J->max_pages) { return -1; }"),
     "reader_bf16_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;"),
@@ -59,6 +59,10 @@ MUTANTS = {
                             "out[ORACLE_D + j] = 0;"),
     "nan_sign_dropped": ("pthread_once(&g_table_once, build_table);\n  uint8_t sign = signbit(x) ? 0x80 : 0x00;\n  if (isnan(x)) return (uint8_t)(sign | 0x7F);",
                          "pthread_once(&g_table_once, build_table);\n  uint8_t sign = signbit(x) ? 0x80 : 0x00;\n  if (isnan(x)) return (uint8_t)0x7F;"),
+    "scaled_nan_sign_from_quotient": ("q[i] = isnan(v[i]) ? oracle_e4m3_encode(v[i]) : oracle_e4m3_encode(v[i] / s);",
+                                      "q[i] = oracle_e4m3_encode(isnan(v[i]) ? fabsf(v[i]) : v[i] / s);"),
+    "q8_nan_sign_dropped": ("q8[i * d + j] = isnan(v[j]) ? oracle_e4m3_encode(v[j]) : oracle_e4m3_encode(v[j] / s);",
+                            "q8[i * d + j] = isnan(v[j]) ? (uint8_t)0x7F : oracle_e4m3_encode(v[j] / s);"),
 }
 
 
