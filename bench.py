@@ -2,16 +2,20 @@
 """Benchmark of the sparse FP8 MLA attention hot path on GB300.
 
 One step = one pass of the hot path over one batch of the chosen workload:
-the fused BF16 -> FP8 KV writer stores the batch's new latent rows, then the
-sparse attention call (index translation, row gather, dequantisation, QK^T,
-softmax, PV, split-K merge) produces O and LSE for every query token.
-The prefill workload also quantises its queries to FP8 on the GPU first.
+the fused BF16 -> FP8 KV writer stores the batch's new latent rows, the
+prefill batch quantises its queries to FP8, then the sparse attention call
+(index translation, row gather, dequantisation, QK^T, softmax, PV, split-K
+merge) produces O and LSE for every query token.
 
-Default workload: decode_raw512 (64 query tokens, 16 heads, top-k 2048 over
-a 131072-row raw FP8 pool, page size 64).  L2 is flushed (a 2x-L2 buffer is
-written) before every timed step; steps are timed with CUDA events on the
-launching stream at the step boundaries, and the attention call alone (for the
-roofline) in a second loop with the same flush.  Prints one JSON line (rank 0).
+Default workload (the headline line): prefill_q8_raw512, the largest batch
+(4096 query tokens, 32 heads, FP8 queries, top-k 2048 over a 16384-row raw
+FP8 pool, page size 64).  L2 is flushed (a 2x-L2 buffer is written) before
+every timed step and every timed call.  Timing: CUDA events on the launching
+stream; the K timed steps give `value`; the attention call alone is timed in
+5 runs of K calls (median of the runs' mean call time) for the roofline.
+`per_config` carries every other workload measured the same way (decode
+batches, writers, the writer sweep, the reader), each with its roofline.
+Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference   # the CPU oracle timed on the host cores
@@ -46,39 +50,61 @@ ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_tc.cu",
                 "sparse_mla_attention_page_gb300/csrc/combine.cu"]
 ATTN_KERNEL = "sparse_attn_tc_kernel + combine_kernel (the attention call)"
 COMPUTE_DTYPE = "e4m3"         # tcgen05 kind::f8f6f4 MMAs (E4M3 operands, FP32 accumulation)
-
+RUNS = 5                       # runs per roofline figure (median of the runs' mean call time)
 
 ROW_BYTES = {"raw512": 512, "scaled528": 528, "rope656": 656}
 WRITERS = {"raw512": lambda b: b.dsa_kv_write_raw, "scaled528": lambda b: b.dsa_kv_write_scaled,
            "rope656": lambda b: b.dsa_kv_write_rope656}
 
+# per_config entries: (key, kind, workload, options)
+PER_CONFIG = [
+    ("tiny_decode_raw512", "attention", "tiny_decode_raw512", {}),
+    ("decode_raw512", "attention", "decode_raw512", {}),
+    ("decode_scaled528", "attention", "decode_scaled528", {}),
+    ("prefill_q8_raw512", "attention", "prefill_q8_raw512", {}),
+    ("kv_write_raw512", "kv_write", None, {"layout": "raw512"}),
+    ("kv_write_scaled528", "kv_write", None, {"layout": "scaled528"}),
+    ("writer_sweep_raw512_h8", "attention", "writer_sweep", {"heads": 8, "layout": "raw512"}),
+    ("writer_sweep_raw512_h16", "attention", "writer_sweep", {"heads": 16, "layout": "raw512"}),
+    ("writer_sweep_raw512_h32", "attention", "writer_sweep", {"heads": 32, "layout": "raw512"}),
+    ("writer_sweep_scaled528_h8", "attention", "writer_sweep", {"heads": 8, "layout": "scaled528"}),
+    ("writer_sweep_scaled528_h16", "attention", "writer_sweep", {"heads": 16, "layout": "scaled528"}),
+    ("writer_sweep_scaled528_h32", "attention", "writer_sweep", {"heads": 32, "layout": "scaled528"}),
+    ("decode_rope656", "attention", "decode_rope656", {}),
+    ("prefill_q8_scaled528", "attention", "prefill_q8_scaled528", {}),
+    ("kv_write_rope656", "kv_write", None, {"layout": "rope656"}),
+    ("gather_dequant_decode_raw512", "gather_dequant", "decode_raw512", {}),
+    ("gather_dequant_decode_scaled528", "gather_dequant", "decode_scaled528", {}),
+    ("gather_dequant_tiny_decode_raw512", "gather_dequant", "tiny_decode_raw512", {}),
+]
 
-def parse_args():
+
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=list(W.WORKLOADS), default="decode_raw512")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--workload", choices=list(W.WORKLOADS), default="prefill_q8_raw512")
+    p.add_argument("--cpu-seconds", type=float, default=8.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=300)
-    p.add_argument("--op", choices=["attention", "gather_dequant", "kv_write"], default="attention",
-                   help="gather_dequant times the BF16 reader over the workload's top-k lists instead; "
-                        "kv_write times one KV writer on 16384 new rows into a 262144-row pool")
+    p.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
+    p.add_argument("--only", default=None,
+                   help="comma-separated per_config keys to time (default: all)")
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--layout", choices=["raw512", "scaled528", "rope656"], default="raw512",
-                   help="row layout of --op kv_write and of --workload writer_sweep (raw512, scaled528)")
+                   help="row layout of --workload writer_sweep (raw512, scaled528)")
     p.add_argument("--heads", type=int, default=16, help="head count of --workload writer_sweep")
     p.add_argument("--warm", action="store_true",
                    help="informational: no L2 flush between steps (inputs may stay in L2); "
                         "the default run flushes before every step")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 # ----------------------------------------------------------------- workloads
 
 def make_workload(name: str, heads: int = 16, layout: str = "raw512") -> dict:
-    if name == "writer_sweep":   # decode over freshly written rows: --heads, --layout
+    if name == "writer_sweep":   # decode over freshly written rows: heads, layout
         if layout not in ("raw512", "scaled528"):
             raise SystemExit("writer_sweep takes --layout raw512 or scaled528")
         return W.writer_sweep(H=heads, layout=layout)
@@ -95,13 +121,17 @@ def step_rows(w: dict) -> tuple[np.ndarray, np.ndarray]:
     return x, slots
 
 
+def is_prefill(w: dict) -> bool:
+    return w["name"].startswith("prefill_q8")
+
+
 def algorithmic_bytes(w: dict) -> int:
     """Bytes the attention call must move: each valid entry's row once, plus the
     query, q_scale, top-k list, O and LSE."""
     T, H, K = w["T"], w["H"], w["K"]
     R = ROW_BYTES[w["layout"]]
     valid = W.valid_entry_count(w["topk"])
-    q8 = w["name"].startswith("prefill_q8")
+    q8 = is_prefill(w)
     q_width = 576 if w["layout"] == "rope656" else 512
     q_bytes = T * H * q_width * (1 if q8 else 2) + (T * H * 4 if q8 else 0)
     return valid * R + q_bytes + T * K * 4 + T * H * 512 * 2 + T * H * 4
@@ -113,97 +143,22 @@ def attn_flops(w: dict) -> int:
     return 2 * w["H"] * (dk + 512) * W.valid_entry_count(w["topk"])
 
 
-def run_gather(args) -> dict:
-    """The gather/dequantise reader over the workload's pool and top-k lists:
-    CUDA events around each call, L2 flushed before every call."""
-    import torch
-
-    from sparse_mla_attention_page_gb300 import binding
-    dev = torch.device("cuda", 0)
-    w = make_workload(args.workload, args.heads, args.layout)
-    T, K, layout = w["T"], w["K"], w["layout"]
-    R = 512 if layout == "raw512" else 528
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
-    pool = torch.zeros(w["pool_rows"], R, dtype=torch.uint8, device=dev)
-    (binding.dsa_kv_write_raw if layout == "raw512" else binding.dsa_kv_write_scaled)(
-        bf(w["kv_src"]), torch.from_numpy(w["kv_slots"]).to(dev), pool)
-    topk = torch.from_numpy(w["topk"]).to(dev)
-    pt = None if w["page_table"] is None else torch.from_numpy(w["page_table"]).to(dev)
-    out = torch.empty(T * K, 512, dtype=torch.bfloat16, device=dev)
-    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
-    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 256 << 20),
-                        dtype=torch.uint8, device=dev)
-    call = lambda: binding.dsa_gather_dequant(pool, layout, topk, out, idx, page_table=pt,  # noqa: E731
-                                              page_size=w["page_size"])
-    for _ in range(args.warmup):
-        flush.zero_()
-        call()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record()
-        call()
-        ev[i][1].record()
-    torch.cuda.synchronize(dev)
-    us = float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) * 1e3
-    valid = W.valid_entry_count(w["topk"])
-    abytes = valid * R + valid * 1024 + T * K * 8
-    peak = float(measured_peaks().get("hbm_gbs", FALLBACK_HBM_GBS))
-    achieved = abytes / (us * 1e-6) / 1e9
-    return {"metric": "gather-dequant selected rows/s and HBM GB/s (fraction of GB300 roofline)",
-            "value": round(valid / (us * 1e-6), 1), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "us_per_call": round(us, 3), "higher_is_better": True,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "op": "gather_dequant", "T": T, "K": K, "layout": layout,
-                       "valid_entries": valid, "l2": "flushed before every call"},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "algorithmic_bytes_per_call": abytes}}
+def gather_bytes(w: dict) -> int:
+    """Bytes the reader must move: per valid entry its row and its BF16 output row
+    (selected branch), or every pool row in and out once (full-pool branch), plus
+    the top-k list read and the remapped list written."""
+    T, K, R = w["T"], w["K"], ROW_BYTES[w["layout"]]
+    width = 576 if w["layout"] == "rope656" else 512
+    if T * K < w["pool_rows"]:
+        rows = W.valid_entry_count(w["topk"])
+    else:
+        rows = w["pool_rows"]
+    return rows * (R + 2 * width) + T * K * 8
 
 
-def run_kv_write(args) -> dict:
-    """One fused BF16 -> FP8 KV writer on 16384 new rows (N(0,1) x U(0.1, 8)) into
-    distinct random slots of a 262144-row pool: CUDA events around each call,
-    L2 flushed before every call."""
-    import torch
-
-    from sparse_mla_attention_page_gb300 import binding
-    dev = torch.device("cuda", 0)
-    w = W.writer_rows()
-    layout, n = args.layout, w["n_rows"]
-    x = w["x_bf16"]
-    if layout == "rope656":   # 576-wide input rows: 512 latent dims + 64 RoPE dims
-        rope = W.f32_to_bf16_bits(W.rng_for(8).standard_normal((n, W.D_ROPE), dtype=np.float32))
-        x = np.concatenate([x, rope], axis=1)
-    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
-    slots = torch.from_numpy(w["slots"]).to(dev)
-    pool = torch.zeros(w["pool_rows"], ROW_BYTES[layout], dtype=torch.uint8, device=dev)
-    write = WRITERS[layout](binding)
-    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 256 << 20),
-                        dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
-        flush.zero_()
-        write(xd, slots, pool)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record()
-        write(xd, slots, pool)
-        ev[i][1].record()
-    torch.cuda.synchronize(dev)
-    us = float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) * 1e3
-    abytes = n * (x.shape[1] * 2 + ROW_BYTES[layout] + 8)     # BF16 row in, FP8 row out, slot
-    peak = float(measured_peaks().get("hbm_gbs", FALLBACK_HBM_GBS))
-    achieved = abytes / (us * 1e-6) / 1e9
-    return {"metric": "KV writer rows/s and HBM GB/s (fraction of GB300 roofline)",
-            "value": round(n / (us * 1e-6), 1), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "us_per_call": round(us, 3), "higher_is_better": True,
-            "dtype": "e4m3", "data": "synthetic",
-            "config": {"op": "kv_write", "layout": layout, "n_rows": n, "pool_rows": w["pool_rows"],
-                       "slots": "distinct, uniform over the pool", "l2": "flushed before every call"},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "algorithmic_bytes_per_call": abytes}}
+def writer_bytes(n: int, layout: str) -> int:
+    width = 576 if layout == "rope656" else 512
+    return n * (width * 2 + ROW_BYTES[layout] + 8)     # BF16 row in, FP8 row out, slot
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -239,7 +194,7 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(key: str):
     """DRAM bytes per attention call from a committed ncu summary, only while the
     kernel source is the one that was profiled."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -247,10 +202,49 @@ def recorded_traffic(workload: str):
         return None
     with open(path) as f:
         rec = json.load(f)
-    e = rec.get(workload)
+    e = rec.get(key)
     if not e or e.get("source_sha") != kernel_source_sha():
         return None
     return e.get("dram_bytes_per_call")
+
+
+# -------------------------------------------------------------------- peaks
+
+def measure_fp8_peak(dev) -> dict | None:
+    """Dense FP8 (E4M3 x E4M3 -> BF16) throughput of one 8192^3 GEMM through
+    torch._scaled_mm, best of 10 after warm-up (a burst figure, like the
+    measured BF16 peak)."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()     # column-major operand
+        one = torch.ones((), dtype=torch.float32, device=dev)
+
+        def mm():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            mm()
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        del a, b
+        return {"tflops": round(2 * n ** 3 / min(ts) / 1e12, 1),
+                "how": "torch._scaled_mm E4M3 x E4M3 -> BF16, 8192^3, best of 10 (burst)"}
+    except Exception as e:  # noqa: BLE001 - report and fall back to the nominal ratio
+        return {"tflops": None, "how": f"not measured ({type(e).__name__}: {e})"[:200]}
+
+
+def tensor_peak(peaks: dict, fp8: dict | None) -> tuple[float, str]:
+    if fp8 and fp8.get("tflops"):
+        return float(fp8["tflops"]), "measured FP8 burst"
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    return 2.0 * bf16, "2 x BF16 burst (nominal FP8/BF16 ratio)"
 
 
 # -------------------------------------------------------------------- clocks
@@ -267,7 +261,7 @@ class ClockSampler:
         self.gpu_id = gpu_id
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
         if self.gpu_id is not None:
             cmd += ["-i", self.gpu_id]
         try:
@@ -304,6 +298,189 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
+class Timer:
+    """CUDA-event timing of one call per step on the launching stream, with an
+    L2 flush (a write of twice the L2 size) before every step."""
+
+    def __init__(self, dev, warm: bool = False):
+        import torch
+        self.torch = torch
+        self.dev = dev
+        self.warm = warm
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush(self):
+        if not self.warm:
+            self.flush_buf.zero_()
+
+    def run(self, fn, steps: int) -> list:
+        """Per-step milliseconds of `steps` flushed calls of fn."""
+        torch = self.torch
+        stream = torch.cuda.current_stream(self.dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            self.flush()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(self.dev)
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    def median_call_us(self, fn, steps: int, warmup: int, runs: int = RUNS) -> tuple[float, list]:
+        """Median over `runs` runs of the mean flushed call time (microseconds)."""
+        for _ in range(warmup):
+            self.flush()
+            fn()
+        self.torch.cuda.synchronize(self.dev)
+        means = [statistics.mean(self.run(fn, steps)) * 1e3 for _ in range(runs)]
+        return statistics.median(means), [round(m, 3) for m in means]
+
+
+class AttnCase:
+    """Device state of one attention workload: the pool filled by the GPU writer,
+    the step's new rows, queries, lists and outputs; `write()` is the step's
+    writer (+ FP8 query quantiser for prefill), `attn()` the attention call."""
+
+    def __init__(self, w: dict, dev, binding):
+        import torch
+        self.w, self.dev, self.b = w, dev, binding
+        T, H, K = w["T"], w["H"], w["K"]
+        self.layout = w["layout"]
+        self.prefill = is_prefill(w)
+
+        def to_dev(a, dtype=None):
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            return (t.view(dtype) if dtype is not None else t).to(dev)
+
+        self.to_dev = to_dev
+        self.bf16 = lambda a: to_dev(a.view(np.int16), torch.bfloat16)
+        self.writer = WRITERS[self.layout](binding)
+        self.pool = torch.zeros(w["pool_rows"], ROW_BYTES[self.layout], dtype=torch.uint8, device=dev)
+        kv_src = self.bf16(w["kv_src"])
+        self.writer(kv_src, to_dev(w["kv_slots"]), self.pool)
+        del kv_src
+        self.x_new_h, self.slots_h = step_rows(w)
+        self.x_new, self.slots = self.bf16(self.x_new_h), to_dev(self.slots_h)
+        self.q = self.bf16(w["q_bf16"])
+        self.topk = to_dev(w["topk"])
+        self.pt = None if w["page_table"] is None else to_dev(w["page_table"])
+        self.o = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+        self.ws = binding.workspace_for(T, H, K, device=dev)
+        self.q8 = torch.empty(T, H, 512, dtype=torch.uint8, device=dev) if self.prefill else None
+        self.qs = torch.empty(T, H, dtype=torch.float32, device=dev) if self.prefill else None
+        if self.prefill:
+            binding.dsa_quantize_q8(self.q, self.q8, self.qs)
+
+    def write(self):
+        self.writer(self.x_new, self.slots, self.pool)
+        if self.prefill:
+            self.b.dsa_quantize_q8(self.q, self.q8, self.qs)
+
+    def attn(self):
+        w = self.w
+        if self.prefill:
+            self.b.dsa_sparse_attn_prefill_q8(self.q8, self.qs, self.pool, self.layout, self.topk, w["sm_scale"],
+                                              self.o, self.lse, self.ws, page_table=self.pt,
+                                              page_size=w["page_size"])
+        else:
+            self.b.dsa_sparse_attn_decode(self.q, self.pool, self.layout, self.topk, w["sm_scale"], self.o,
+                                          self.lse, self.ws, page_table=self.pt, page_size=w["page_size"])
+
+    def step(self):
+        self.write()
+        self.attn()
+
+    def launches_per_step(self) -> int:
+        # writer, [q8 quantiser], attention, [split-unit merge when a unit spans CTAs]
+        return 1 + (1 if self.prefill else 0) + 1 + (1 if self.ws is not None else 0)
+
+
+def attn_roofline(w: dict, us: float, peaks: dict, tpeak: float, tsrc: str, traffic) -> dict:
+    """Both rooflines of one attention call; `bound` names the binding one: HBM
+    for the decode batches, the tensor pipe for the prefill batches (their pools
+    sit in L2, so algorithmic HBM bytes there overstate what DRAM must move)."""
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    abytes = algorithmic_bytes(w)
+    gbs = abytes / (us * 1e-6) / 1e9
+    tfl = attn_flops(w) / (us * 1e-6) / 1e12
+    bound = "tensor" if is_prefill(w) else "hbm"
+    main = ({"achieved": round(tfl, 2), "peak": tpeak, "unit": "TFLOP/s", "frac": round(tfl / tpeak, 4)}
+            if bound == "tensor" else
+            {"achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)})
+    return {"bound": bound, **main, "traffic": traffic, "kernel": ATTN_KERNEL,
+            "algorithmic_bytes_per_call": abytes, "algorithmic_flops_per_call": attn_flops(w),
+            "attn_us_per_call": round(us, 3),
+            "hbm": {"achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                    "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+            "tensor": {"achieved": round(tfl, 2), "peak": tpeak, "unit": "TFLOP/s",
+                       "frac": round(tfl / tpeak, 4), "peak_source": tsrc}}
+
+
+def per_config_attention(key, w, dev, binding, timer, args, peaks, tpeak, tsrc) -> dict:
+    case = AttnCase(w, dev, binding)
+    steps = max(5, min(args.steps, 20))
+    us, runs = timer.median_call_us(case.attn, steps, args.warmup)
+    step_ms = timer.run(case.step, steps)
+    roof = attn_roofline(w, us, peaks, tpeak, tsrc, recorded_traffic(key))
+    return {"value": round(w["T"] * len(step_ms) / (sum(step_ms) / 1e3), 1), "unit": UNIT,
+            "workload": w["name"], "T": w["T"], "H": w["H"], "K": w["K"], "layout": w["layout"],
+            "pool_rows": w["pool_rows"], "valid_entries": W.valid_entry_count(w["topk"]),
+            "attn_us_per_call": round(us, 3), "attn_us_runs": runs,
+            "step_us": round(statistics.mean(step_ms) * 1e3, 3), "roofline": roof}
+
+
+def per_config_kv_write(layout, dev, binding, timer, args, peaks) -> dict:
+    """One fused BF16 -> FP8 KV writer on 16384 new rows (N(0,1) x U(0.1, 8)) into
+    distinct random slots of a 262144-row pool."""
+    import torch
+    w = W.writer_rows()
+    n = w["n_rows"]
+    x = w["x_bf16"]
+    if layout == "rope656":   # 576-wide input rows: 512 latent dims + 64 RoPE dims
+        rope = W.f32_to_bf16_bits(W.rng_for(8).standard_normal((n, W.D_ROPE), dtype=np.float32))
+        x = np.concatenate([x, rope], axis=1)
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    slots = torch.from_numpy(w["slots"]).to(dev)
+    pool = torch.zeros(w["pool_rows"], ROW_BYTES[layout], dtype=torch.uint8, device=dev)
+    write = WRITERS[layout](binding)
+    us, runs = timer.median_call_us(lambda: write(xd, slots, pool), max(5, min(args.steps, 20)), args.warmup)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    abytes = writer_bytes(n, layout)
+    gbs = abytes / (us * 1e-6) / 1e9
+    return {"value": round(n / (us * 1e-6), 1), "unit": "rows/s", "op": "kv_write", "layout": layout,
+            "n_rows": n, "pool_rows": w["pool_rows"], "us_per_call": round(us, 3), "us_runs": runs,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "algorithmic_bytes_per_call": abytes,
+                         "kernel": "kv_write_*_kernel"}}
+
+
+def per_config_gather(w, dev, binding, timer, args, peaks) -> dict:
+    """The gather/dequantise reader over a workload's pool and lists."""
+    import torch
+    case = AttnCase(w, dev, binding)
+    T, K = w["T"], w["K"]
+    out = binding.gather_workspace_for(T, K, w["pool_rows"], w["layout"], device=dev)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+
+    def call():
+        binding.dsa_gather_dequant(case.pool, w["layout"], case.topk, out, idx, page_table=case.pt,
+                                   page_size=w["page_size"])
+    us, runs = timer.median_call_us(call, max(5, min(args.steps, 20)), args.warmup)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    abytes = gather_bytes(w)
+    gbs = abytes / (us * 1e-6) / 1e9
+    return {"value": round(W.valid_entry_count(w["topk"]) / (us * 1e-6), 1), "unit": "entries/s",
+            "op": "gather_dequant", "workload": w["name"], "T": T, "K": K, "layout": w["layout"],
+            "pool_rows": w["pool_rows"], "branch": "selected" if T * K < w["pool_rows"] else "full pool",
+            "workspace_bytes": binding.dsa_gather_dequant_workspace_bytes(T, K, w["pool_rows"], w["layout"]),
+            "us_per_call": round(us, 3), "us_runs": runs,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "algorithmic_bytes_per_call": abytes,
+                         "kernel": "gather_dequant_kernel"}}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int, dist):
     import torch
 
@@ -314,58 +491,14 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     w = make_workload(args.workload, args.heads, args.layout)
     T, H, K = w["T"], w["H"], w["K"]
     layout = w["layout"]
-    prefill = w["name"].startswith("prefill_q8")
-
-    def to_dev(a, dtype=None):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.view(dtype) if dtype is not None else t).to(dev)
-
-    def bf16(a):
-        return to_dev(a.view(np.int16), torch.bfloat16)
-
-    write = WRITERS[layout](binding)
-    pool = torch.zeros(w["pool_rows"], ROW_BYTES[layout], dtype=torch.uint8, device=dev)
-    kv_src = bf16(w["kv_src"])
-    write(kv_src, to_dev(w["kv_slots"]), pool)
-    del kv_src
-    x_new_h, slots_h = step_rows(w)
-    x_new, slots = bf16(x_new_h), to_dev(slots_h)
-    q = bf16(w["q_bf16"])
-    topk = to_dev(w["topk"])
-    pt = None if w["page_table"] is None else to_dev(w["page_table"])
-    o = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
-    ws = binding.workspace_for(T, H, K, device=dev)
-    q8 = torch.empty(T, H, 512, dtype=torch.uint8, device=dev) if prefill else None
-    qs = torch.empty(T, H, dtype=torch.float32, device=dev) if prefill else None
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    prefill = is_prefill(w)
+    timer = Timer(dev, args.warm)
     stream = torch.cuda.current_stream(dev)
-
-    def flush():
-        if not args.warm:
-            flush_buf.zero_()
-
-    def step_write():
-        write(x_new, slots, pool)
-        if prefill:
-            binding.dsa_quantize_q8(q, q8, qs)
-
-    def step_attn():
-        if prefill:
-            binding.dsa_sparse_attn_prefill_q8(q8, qs, pool, layout, topk, w["sm_scale"], o, lse, ws,
-                                               page_table=pt, page_size=w["page_size"])
-        else:
-            binding.dsa_sparse_attn_decode(q, pool, layout, topk, w["sm_scale"], o, lse, ws,
-                                           page_table=pt, page_size=w["page_size"])
-
-    # writer, [q8 quantiser], attention, [split-unit merge when a unit spans CTAs]
-    launches_per_step = 1 + (1 if prefill else 0) + 1 + (1 if ws is not None else 0)
+    case = AttnCase(w, dev, binding)
 
     for _ in range(args.warmup):
-        flush()
-        step_write()
-        step_attn()
+        timer.flush()
+        case.step()
     torch.cuda.synchronize(dev)
 
     props = torch.cuda.get_device_properties(dev)
@@ -375,36 +508,20 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     sampler = ClockSampler(gpu_id)
     sampler.start()
     time.sleep(0.3)
-    # whole steps, events at the step boundaries only: the attention kernel is a
-    # programmatic dependent launch and may start its set-up while the writer runs
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    # the K timed steps, events at the step boundaries only: the attention kernel is
+    # a programmatic dependent launch and may start its set-up while the writer runs
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    for i in range(args.steps):
-        flush()
-        ev[i][0].record(stream)
-        step_write()
-        step_attn()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms = timer.run(case.step, args.steps)
     if dist is not None:
         dist.barrier()
-    # the attention call alone (its kernels' duration, for the roofline): same
-    # L2 flush before every call, the inputs of the last step
-    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush()
-        ev_a[i][0].record(stream)
-        step_attn()
-        ev_a[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    # the attention call alone, for the roofline: RUNS runs of K flushed calls
+    attn_us, attn_runs = timer.median_call_us(case.attn, args.steps, 0)
     t_wall1 = time.time()
     time.sleep(0.2)
     sampler.stop()
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    attn_ms = [e[0].elapsed_time(e[1]) for e in ev_a]
     total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
 
     # end to end through the public API: the step's inputs from one pinned host
@@ -418,7 +535,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
         return offs, n
 
     in_parts = [np.ascontiguousarray(w["q_bf16"]), np.ascontiguousarray(w["topk"]),
-                np.ascontiguousarray(x_new_h), np.ascontiguousarray(slots_h)]
+                np.ascontiguousarray(case.x_new_h), np.ascontiguousarray(case.slots_h)]
     if w["page_table"] is not None:
         in_parts.append(np.ascontiguousarray(w["page_table"]))
     in_offs, in_n = packed(in_parts)
@@ -433,8 +550,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
 
     q_e = view(d_in, in_offs[0], w["q_bf16"].shape, torch.bfloat16)
     topk_e = view(d_in, in_offs[1], w["topk"].shape, torch.int32)
-    x_e = view(d_in, in_offs[2], x_new_h.shape, torch.bfloat16)
-    slots_e = view(d_in, in_offs[3], slots_h.shape, torch.int64)
+    x_e = view(d_in, in_offs[2], case.x_new_h.shape, torch.bfloat16)
+    slots_e = view(d_in, in_offs[3], case.slots_h.shape, torch.int64)
     pt_e = None if w["page_table"] is None else view(d_in, in_offs[4], w["page_table"].shape, torch.int32)
     (o_off, lse_off), out_n = packed([np.empty((T, H, 512), np.uint16), np.empty((T, H), np.float32)])
     d_out = torch.empty(out_n, dtype=torch.uint8, device=dev)
@@ -444,36 +561,36 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     if prefill:
         q8_e = torch.empty(T, H, 512, dtype=torch.uint8, device=dev)
         qs_e = torch.empty(T, H, dtype=torch.float32, device=dev)
-    h2d, d2h = in_n, out_n
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
     for i in range(n_e2e + 3):
-        flush()
+        timer.flush()
         if i >= 3:
             e2e_ev[i - 3][0].record(stream)
         d_in.copy_(h_in, non_blocking=True)
-        write(x_e, slots_e, pool)
+        case.writer(x_e, slots_e, case.pool)
         if prefill:
             binding.dsa_quantize_q8(q_e, q8_e, qs_e)
-            binding.dsa_sparse_attn_prefill_q8(q8_e, qs_e, pool, layout, topk_e, w["sm_scale"], o_e, lse_e, ws,
-                                               page_table=pt_e, page_size=w["page_size"])
+            binding.dsa_sparse_attn_prefill_q8(q8_e, qs_e, case.pool, layout, topk_e, w["sm_scale"], o_e, lse_e,
+                                               case.ws, page_table=pt_e, page_size=w["page_size"])
         else:
-            binding.dsa_sparse_attn_decode(q_e, pool, layout, topk_e, w["sm_scale"], o_e, lse_e, ws,
+            binding.dsa_sparse_attn_decode(q_e, case.pool, layout, topk_e, w["sm_scale"], o_e, lse_e, case.ws,
                                            page_table=pt_e, page_size=w["page_size"])
         h_out.copy_(d_out, non_blocking=True)
         if i >= 3:
             e2e_ev[i - 3][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(float(sum(e[0].elapsed_time(e[1]) for e in e2e_ev)), dist, dev)
+    del d_in, h_in, d_out, h_out
 
     if rank != 0:
         return None
     peaks = measured_peaks()
-    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    attn_mean_s = statistics.mean(attn_ms) / 1e3
-    abytes = algorithmic_bytes(w)
-    achieved = abytes / attn_mean_s / 1e9
-    traffic = recorded_traffic(args.workload)
+    fp8 = measure_fp8_peak(dev)
+    tpeak, tsrc = tensor_peak(peaks, fp8)
+    traffic = recorded_traffic(args.workload if args.workload != "writer_sweep" else None)
+    roof = attn_roofline(w, attn_us, peaks, tpeak, tsrc, traffic)
+    roof["attn_us_runs"] = attn_runs
     value = world * T * args.steps / (total_ms / 1e3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -485,24 +602,49 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
                    "valid_entries": W.valid_entry_count(w["topk"]),
                    "step": ("quantize_q8 + " if prefill else "") + f"kv_write_{layout[:3]} of {T} new rows + sparse attention",
                    "l2": ("not flushed (warm; informational)" if args.warm
-                          else f"flushed before every step ({flush_buf.numel() >> 20} MiB write)"),
+                          else f"flushed before every step ({timer.flush_buf.numel() >> 20} MiB write)"),
+                   "timing": f"value: {args.steps} timed steps; roofline: median of {RUNS} runs of "
+                             f"{args.steps} flushed calls",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ATTN_KERNEL, "algorithmic_bytes_per_call": abytes,
-                     "attn_us_per_call": round(attn_mean_s * 1e6, 3),
-                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
-                     "tensor_tflops": round(attn_flops(w) / attn_mean_s / 1e12, 2),
-                     # FP8 dense peak = measured BF16 burst x the nominal FP8/BF16 ratio (2)
-                     "tensor_peak_tflops": round(2.0 * float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), 1),
-                     "tensor_frac": round(attn_flops(w) / attn_mean_s / 1e12
-                                          / (2.0 * float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))), 4)},
+        "roofline": roof,
         "e2e": {"value": round(world * T * n_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+                "h2d_bytes_per_step": in_n, "d2h_bytes_per_step": out_n},
+        "gpu_launches": case.launches_per_step() * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
+        "fp8_peak": fp8,
     }
+    del case
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_per_config:
+        line["per_config"] = run_per_config(args, dev, binding, timer, peaks, tpeak, tsrc,
+                                            headline=(args.workload, roof, value))
     return line, w
+
+
+def run_per_config(args, dev, binding, timer, peaks, tpeak, tsrc, headline) -> dict:
+    import torch
+    only = None if args.only is None else set(args.only.split(","))
+    out = {}
+    for key, kind, wname, opt in PER_CONFIG:
+        if only is not None and key not in only:
+            continue
+        if kind == "attention" and wname == headline[0] and not opt:
+            out[key] = {"same_as": "headline line (roofline, value)"}
+            continue
+        t0 = time.time()
+        try:
+            if kind == "attention":
+                w = make_workload(wname, opt.get("heads", 16), opt.get("layout", "raw512"))
+                out[key] = per_config_attention(key, w, dev, binding, timer, args, peaks, tpeak, tsrc)
+            elif kind == "kv_write":
+                out[key] = per_config_kv_write(opt["layout"], dev, binding, timer, args, peaks)
+            else:
+                out[key] = per_config_gather(make_workload(wname), dev, binding, timer, args, peaks)
+        except Exception as e:  # noqa: BLE001 - one failing config must not hide the others
+            out[key] = {"error": f"{type(e).__name__}: {e}"[:300]}
+        out[key]["wall_s"] = round(time.time() - t0, 1)
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------- oracle
@@ -523,33 +665,46 @@ def oracle_setup(w: dict):
     import oracle
     pool = oracle.fill_pool(w)
     q8 = qs = None
-    if w["name"].startswith("prefill_q8"):
+    if is_prefill(w):
         q8, qs = oracle.quantize_q8(w["q_bf16"])
     return pool, q8, qs
 
 
-def cpu_baseline(w: dict, seconds: float) -> dict:
-    """The oracle as it stands, on all host cores, over whole passes of the
-    batch (writer of the step's new rows + attention for every token) until
-    ``seconds`` have passed; for the prefill batch a 64-token slice per pass."""
+def _oracle_rate(w, pool, q8, qs, n_threads: int, seconds: float, chunk: int):
+    """Query-tokens/s of the oracle (writer of the step's rows + attention) over
+    consecutive slices of `chunk` tokens until `seconds` have passed."""
     import oracle
-    cores = len(os.sched_getaffinity(0))
-    pool, q8, qs = oracle_setup(w)
     x_new, slots = step_rows(w)
     T = w["T"]
-    tokens = np.arange(min(T, 64)) if w["name"].startswith("prefill_q8") else np.arange(T)
-    done = 0
+    done, start = 0, 0
     t0 = time.perf_counter()
     while True:
+        tokens = (np.arange(chunk) + start) % T
+        start = (start + chunk) % T
         oracle.kv_write(w["layout"], x_new, slots, pool)
-        oracle_pass(w, pool, tokens, cores, q8, qs)
-        done += len(tokens)
+        oracle_pass(w, pool, tokens, n_threads, q8, qs)
+        done += chunk
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(w: dict, seconds: float) -> dict:
+    """The oracle as it stands on the host cores: all cores (the figure) and one
+    thread, each over slices of the batch until its time has passed; each slice
+    runs the writer of the step's new rows and the attention of its tokens."""
+    cores = len(os.sched_getaffinity(0))
+    pool, q8, qs = oracle_setup(w)
+    T = w["T"]
+    chunk_all = min(T, 64) if is_prefill(w) else T
+    done, dt = _oracle_rate(w, pool, q8, qs, cores, seconds, chunk_all)
+    chunk_one = min(T, 2 if is_prefill(w) else 16)
+    done1, dt1 = _oracle_rate(w, pool, q8, qs, 1, seconds / 2, chunk_one)
     return {"value": round(done / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done // len(tokens)} passes x {len(tokens)} tokens of {w['name']} "
-                      f"(writer of the step's rows + float64 attention), {dt:.1f} s"}
+            "sample": f"{done} tokens of {w['name']} in slices of {chunk_all} (writer of the step's rows + "
+                      f"float64 attention), {dt:.1f} s on {cores} threads",
+            "single_thread": {"value": round(done1 / dt1, 3), "unit": UNIT, "cores": 1,
+                              "sample": f"{done1} tokens in slices of {chunk_one}, {dt1:.1f} s on 1 thread"}}
 
 
 def run_reference(args, rank: int):
@@ -604,10 +759,6 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     import importlib
     importlib.import_module("sparse_mla_attention_page_gb300.build").build()
-    if args.op in ("gather_dequant", "kv_write"):
-        if rank == 0:
-            print(json.dumps(run_gather(args) if args.op == "gather_dequant" else run_kv_write(args)), flush=True)
-        return
     out = run_ours(args, rank, world, local_rank, dist)
     if out is not None:
         line, w = out

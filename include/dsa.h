@@ -84,6 +84,19 @@ enum {
 /* Human-readable name of a status code (static string). */
 const char* dsa_status_string(int status);
 
+/* Diagnostics: sets the limit, in nanoseconds, of every bounded wait inside
+ * the attention kernel (default 1 s) for the attention calls made after it,
+ * process-wide, and returns the previous limit.  A wait that runs out makes
+ * the kernel give up: its other waits return at once, it waits (with a
+ * separate 2 s bound) for its own copies and tensor-core operations in
+ * flight, releases its tensor memory, returns, and ORs DSA_DEV_ERR_TIMEOUT
+ * into err_flag_dev; that call's outputs are then not valid, and the CUDA
+ * context stays usable.  A limit of 0 makes the first wait that is not
+ * already complete give up, which lets a test exercise this path without
+ * stalling the GPU.  Not meant to be changed while attention calls are being
+ * issued from other threads. */
+uint64_t dsa_set_wait_limit_ns(uint64_t ns);
+
 /* Bytes of one physical KV row: 512, 528 or 656 ("exported buffer lengths",
  * [P1 Speed Tests and Profiling]); 0 for an unknown layout. */
 size_t dsa_kv_row_bytes(int layout);
@@ -139,9 +152,9 @@ int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* 
 /* ------------------------------------------------------ sparse attention */
 
 /* Workspace bytes the attention entry points need for (T, H, K) on the
- * current device: split-K partial results (two FP32 slots of [heads, 512] and
- * [heads] per SM), needed only when a (token, head group) is spread over
- * several SMs.  May be 0.  Pass at least this many bytes, 256-byte aligned;
+ * current device, for any row layout: split-K partial results (two FP32
+ * slots of [heads, 512] and [heads] per SM), needed only when a (token, head
+ * group) is spread over several SMs.  May be 0.  Pass at least this many bytes, 256-byte aligned;
  * no initialisation is needed: each call writes every byte it reads. */
 size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
 
@@ -173,7 +186,7 @@ size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K);
  *   lse_dev         [T, H] float out.
  *   workspace_dev   ws_bytes >= dsa_sparse_attn_workspace_bytes(T, H, K).
  *   err_flag_dev    nullable int32 error bits.
- * H must be one of 8, 16, 32, 64, 128 (8 or 16 over 656-byte rows).
+ * H must be one of 8, 16, 32, 64, 128.
  * T == 0 is a no-op.
  * Launch: the attention kernel is launched with programmatic stream
  * serialization; it may start its set-up while the previous kernel on the
@@ -209,26 +222,46 @@ int dsa_sparse_attn_prefill_q8(const void* q8_dev, const float* q_scale_dev, int
 
 /* ------------------------------------------- gather / dequantise reader */
 
-/* The rows a top-k list selects, dequantised to BF16 in a buffer padded to
- * one slot per top-k entry, for consumers that attend in BF16 ["[DSA] Support
- * group-scaled FP8 NoPE KV reads for CUDA TileLang", Modifications: the
- * gather/cast reader; P3 review thread: the paged gather with -1 padding].
- * For slot e = t*K + j of entry j of token t:
- *   out[e][d]  = bf16_rn(fp32(e4m3(b_d) * s_g))   (raw rows: s = 1, exact),
- *   idx_out[e] = e for a valid entry, -1 for a masked one (out[e] untouched).
- * Rows resolve exactly as in the attention (page table, token_seq, -1
- * sentinels, the same error bits in err_flag_dev).
- *   pool_dev        [pool_rows, 512 or 528] bytes, 16-byte aligned.
+/* Bytes of the BF16 workspace dsa_gather_dequant writes for T tokens with
+ * top-k width K over a pool of pool_rows rows: min(pool_rows, T*K) rows of
+ * 512 BF16 values (1024 bytes), or of 576 values (1152 bytes) for 656-byte
+ * rows ["[DSA] Support group-scaled FP8 NoPE KV reads for CUDA TileLang",
+ * Modifications: the BF16 payload workspace is bounded by
+ * min(physical_tokens, selected_entries) * 1024 bytes].  The size follows
+ * from the shapes alone, so sizing it needs no device data.  0 for a
+ * negative size or an unknown layout. */
+size_t dsa_gather_dequant_workspace_bytes(int T, int K, int64_t pool_rows, int layout);
+
+/* Gather / dequantise reader: the rows a top-k list selects, dequantised to
+ * BF16 in a workspace that BF16 consumers index with the remapped list
+ * ["[DSA] Support group-scaled FP8 NoPE KV reads for CUDA TileLang",
+ * Modifications: the full and paged readers, int64 physical addressing, the
+ * selected-row workspace with remapped indices and kept masks; P3 review
+ * thread: the paged gather with -1 padding].  Two branches, chosen by shape:
+ *  - T*K < pool_rows (fewer selected entries than physical rows): workspace
+ *    row e = t*K + j holds entry j of token t, idx_out[e] = e;
+ *  - otherwise the whole pool is dequantised: workspace row r holds physical
+ *    row r, idx_out[e] = the entry's physical row.
+ * A masked entry (negative index, or one that fails to resolve, with the
+ * attention's error bits in err_flag_dev) gets idx_out[e] = -1; in the first
+ * branch its workspace row is left untouched.  In both branches
+ * out[idx_out[e]] is entry e's row:
+ *   out[.][d] = bf16_rn(fp32(e4m3(b_d) * s_g))   (raw rows: s = 1, exact),
+ * followed, for 656-byte rows, by the row's 64 RoPE dims as stored.
+ *   pool_dev        [pool_rows, 512, 528 or 656] bytes, 16-byte aligned.
  *   page_table_dev  [B, max_pages] int32, or NULL (indices are physical rows).
  *   token_seq_dev   [T] int32 or NULL.
  *   topk_dev        [T, K] int32, any K >= 1, T * K < 2^31.
- *   out_bf16_dev    [T * K, 512] BF16, 16-byte aligned.
+ *   out_bf16_dev    out_bytes >= dsa_gather_dequant_workspace_bytes(T, K,
+ *                   pool_rows, layout) (else DSA_ERR_WORKSPACE), 16-byte
+ *                   aligned; row-major [rows, 512 or 576] BF16.
  *   idx_out_dev     [T, K] int32.
  * T == 0 is a no-op. */
 int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
                        const int32_t* page_table_dev, int B, int max_pages, int page_size,
                        const int32_t* token_seq_dev, const int32_t* topk_dev, int T, int K,
-                       void* out_bf16_dev, int32_t* idx_out_dev, int32_t* err_flag_dev, void* stream);
+                       void* out_bf16_dev, size_t out_bytes, int32_t* idx_out_dev, int32_t* err_flag_dev,
+                       void* stream);
 
 /* ------------------------------------------- decode without allocation */
 
@@ -249,7 +282,10 @@ int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
  * routine).
  *  - The first call on a device looks up the array's device address for that
  *    device (cudaGetSymbolAddress, with that device current); make that first
- *    call before any stream capture on the device.
+ *    call before any stream capture on the device.  The address is kept for
+ *    the life of the process; after a cudaDeviceReset of that device it is
+ *    stale, so a process that resets a device must not call this entry point
+ *    on it again.
  *  - A (T, H, K) whose workspace (dsa_sparse_attn_workspace_bytes) exceeds
  *    DSA_NOALLOC_SCRATCH_BYTES is refused with DSA_ERR_WORKSPACE, nothing
  *    launched.

@@ -34,7 +34,8 @@ _lib = None
 EXPORTS = (
     "dsa_status_string", "dsa_kv_row_bytes", "dsa_kv_write_raw", "dsa_kv_write_scaled", "dsa_kv_write_rope656",
     "dsa_quantize_q8", "dsa_sparse_attn_workspace_bytes", "dsa_sparse_attn_decode",
-    "dsa_sparse_attn_prefill_q8", "dsa_gather_dequant", "dsa_sparse_attn_decode_noalloc",
+    "dsa_sparse_attn_prefill_q8", "dsa_gather_dequant_workspace_bytes", "dsa_gather_dequant",
+    "dsa_sparse_attn_decode_noalloc", "dsa_set_wait_limit_ns",
 )
 
 
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
             vp, i64, i32 = c.c_void_p, c.c_int64, c.c_int
             L.dsa_status_string.restype = c.c_char_p
             L.dsa_status_string.argtypes = [i32]
+            L.dsa_set_wait_limit_ns.restype = c.c_uint64
+            L.dsa_set_wait_limit_ns.argtypes = [c.c_uint64]
             L.dsa_kv_row_bytes.restype = c.c_size_t
             L.dsa_kv_row_bytes.argtypes = [i32]
             for f in (L.dsa_kv_write_raw, L.dsa_kv_write_scaled, L.dsa_kv_write_rope656):
@@ -80,7 +83,10 @@ def lib() -> ctypes.CDLL:
                 vp, vp, i32, i32, i32, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i32,
                 c.c_float, vp, vp, vp, c.c_size_t, vp, vp]
             L.dsa_gather_dequant.restype = i32
-            L.dsa_gather_dequant.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp]
+            L.dsa_gather_dequant.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, i32, i32, vp, c.c_size_t,
+                                             vp, vp, vp]
+            L.dsa_gather_dequant_workspace_bytes.restype = c.c_size_t
+            L.dsa_gather_dequant_workspace_bytes.argtypes = [i32, i32, i64, i32]
             L.dsa_sparse_attn_decode_noalloc.restype = i32
             L.dsa_sparse_attn_decode_noalloc.argtypes = [
                 vp, i32, i32, i32, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i32,
@@ -115,6 +121,11 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, last: int | None = Non
         raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
     if last is not None and t.shape[-1] != last:
         raise ValueError(f"{name} must have last dimension {last}, got {tuple(t.shape)}")
+
+
+def dsa_set_wait_limit_ns(ns: int) -> int:
+    """Limit of the attention kernel's bounded waits for later calls; returns the old one."""
+    return int(lib().dsa_set_wait_limit_ns(int(ns)))
 
 
 def dsa_kv_row_bytes(layout) -> int:
@@ -205,19 +216,32 @@ def _attn_common(q, pool, layout, topk, o, lse, page_table, token_seq, workspace
     return T, H, lay, B, max_pages, ws_bytes
 
 
+def dsa_gather_dequant_workspace_bytes(T: int, K: int, pool_rows: int, layout) -> int:
+    return int(lib().dsa_gather_dequant_workspace_bytes(T, K, pool_rows, LAYOUTS.get(layout, layout)))
+
+
+def gather_workspace_for(T: int, K: int, pool_rows: int, layout, device=None) -> torch.Tensor:
+    """A BF16 workspace [min(pool_rows, T*K), 512 or 576] for dsa_gather_dequant."""
+    lay = LAYOUTS.get(layout, layout)
+    width = 576 if lay == DSA_KV_ROPE656 else 512
+    rows = min(pool_rows, T * K)
+    return torch.empty(rows, width, dtype=torch.bfloat16, device=device or "cuda")
+
+
 def dsa_gather_dequant(pool, layout, topk, out, idx_out, page_table=None, page_size=64,
                        token_seq=None, err_flag=None, stream=None) -> None:
-    """BF16 rows out [T*K, 512] and remapped indices idx_out [T, K] for topk [T, K]."""
+    """BF16 workspace out [min(pool_rows, T*K), 512 or 576] and remapped indices
+    idx_out [T, K] for topk [T, K]."""
+    lay = LAYOUTS.get(layout, layout)
     _need(pool, "pool", torch.uint8)
     _need(topk, "topk", torch.int32)
-    _need(out, "out", torch.bfloat16, 512)
+    _need(out, "out", torch.bfloat16, 576 if lay == DSA_KV_ROPE656 else 512)
     _need(idx_out, "idx_out", torch.int32)
     if topk.dim() != 2:
         raise ValueError("topk must be [T, K] int32")
     T, K = topk.shape
-    if out.shape[0] < T * K or tuple(idx_out.shape) != (T, K):
-        raise ValueError("out must be [T*K, 512] bf16 and idx_out [T, K] int32")
-    lay = LAYOUTS.get(layout, layout)
+    if tuple(idx_out.shape) != (T, K):
+        raise ValueError("idx_out must be [T, K] int32")
     if page_table is not None:
         _need(page_table, "page_table", torch.int32)
         B, max_pages = page_table.shape
@@ -229,7 +253,8 @@ def dsa_gather_dequant(pool, layout, topk, out, idx_out, page_table=None, page_s
         _need(err_flag, "err_flag", torch.int32)
     _check(lib().dsa_gather_dequant(_ptr(pool), pool.shape[0], lay, _ptr(page_table), B, max_pages,
                                     page_size, _ptr(token_seq), _ptr(topk), T, K, _ptr(out),
-                                    _ptr(idx_out), _ptr(err_flag), _stream(stream)),
+                                    out.numel() * out.element_size(), _ptr(idx_out), _ptr(err_flag),
+                                    _stream(stream)),
            "dsa_gather_dequant")
 
 

@@ -1,6 +1,7 @@
 // C ABI entry points (include/dsa.h): host-side validation, then launches.
 // Every check runs before anything is enqueued; on a non-zero status nothing
 // was launched.
+#include <atomic>
 #include <climits>
 #include <cstdio>
 #include <cstdlib>
@@ -10,9 +11,7 @@
 #include "../../include/dsa.h"
 #include "kernels.h"
 
-namespace {
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+namespace dsa {
 
 // Current device must be compute capability 10.3; returns its SM count.
 int current_device_sms(int* sms) {
@@ -32,6 +31,17 @@ int current_device_sms(int* sms) {
   *sms = count;
   return DSA_OK;
 }
+
+}  // namespace dsa
+
+namespace {
+
+using dsa::current_device_sms;
+
+// Limit of the attention kernel's bounded waits (dsa_set_wait_limit_ns).
+std::atomic<uint64_t> g_wait_ns{1000000000ull};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // A failed launch returns DSA_ERR_CUDA; with DSA_DEBUG set in the environment
 // the CUDA error string is also printed to stderr.
@@ -77,7 +87,7 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   if (D != width || kv_row_dim != width) return DSA_ERR_ROW_WIDTH;
   if (q8 && layout == DSA_KV_ROPE656) return DSA_ERR_LAYOUT;
   if (K <= 0 || K % 128 != 0) return DSA_ERR_TOPK_PAD;
-  if (!heads_ok(H) || (layout == DSA_KV_ROPE656 && H > 16)) return DSA_ERR_HEADS;
+  if (!heads_ok(H)) return DSA_ERR_HEADS;
   if (T == 0) return DSA_OK;
   if (q == nullptr || pool == nullptr || topk == nullptr || o == nullptr || lse == nullptr ||
       (q8 && q_scale == nullptr))
@@ -93,7 +103,7 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   int sms = 0;
   int st = current_device_sms(&sms);
   if (st != DSA_OK) return st;
-  const dsa::AttnPlan plan = dsa::plan_attn(T, H, K, sms);
+  const dsa::AttnPlan plan = dsa::plan_attn(T, H, K, sms, layout == DSA_KV_ROPE656);
   if (plan.ws_bytes > 0) {
     if (ws == nullptr || ws_bytes < plan.ws_bytes) return DSA_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return DSA_ERR_ALIGN;
@@ -127,6 +137,7 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   a.ws_o = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_o_offset) : nullptr;
   a.ws_lse = plan.split ? reinterpret_cast<float*>(wsb + plan.ws_lse_offset) : nullptr;
   a.err = err;
+  a.wait_ns = g_wait_ns.load();
   cudaGetLastError();
   dsa::launch_sparse_attn(a, q8, static_cast<cudaStream_t>(stream));
   return launch_status();
@@ -152,6 +163,8 @@ const char* dsa_status_string(int status) {
     default: return "unknown status";
   }
 }
+
+uint64_t dsa_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
 
 size_t dsa_kv_row_bytes(int layout) {
   if (layout == DSA_KV_RAW512) return 512;
@@ -190,12 +203,19 @@ int dsa_quantize_q8(const void* q_bf16_dev, int64_t n_vec, void* q8_dev, float* 
   return launch_status();
 }
 
+size_t dsa_gather_dequant_workspace_bytes(int T, int K, int64_t pool_rows, int layout) {
+  if (T < 0 || K < 0 || pool_rows < 0 || dsa_kv_row_bytes(layout) == 0) return 0;
+  const size_t width = layout == DSA_KV_ROPE656 ? 576 : 512;
+  return (size_t)dsa::gather_rows(pool_rows, (int64_t)T * K) * width * 2;
+}
+
 int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
                        const int32_t* page_table_dev, int B, int max_pages, int page_size,
                        const int32_t* token_seq_dev, const int32_t* topk_dev, int T, int K,
-                       void* out_bf16_dev, int32_t* idx_out_dev, int32_t* err_flag_dev, void* stream) {
+                       void* out_bf16_dev, size_t out_bytes, int32_t* idx_out_dev, int32_t* err_flag_dev,
+                       void* stream) {
   if (T < 0 || K < 1 || pool_rows < 0) return DSA_ERR_SHAPE;
-  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528) return DSA_ERR_LAYOUT;
+  if (layout != DSA_KV_RAW512 && layout != DSA_KV_SCALED528 && layout != DSA_KV_ROPE656) return DSA_ERR_LAYOUT;
   if (T == 0) return DSA_OK;
   if (pool_dev == nullptr || topk_dev == nullptr || out_bf16_dev == nullptr || idx_out_dev == nullptr)
     return DSA_ERR_NULL;
@@ -204,6 +224,7 @@ int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
     if (B < 1 || max_pages < 1 || page_size < 1) return DSA_ERR_SHAPE;
     if ((int64_t)max_pages * page_size > (int64_t)INT32_MAX + 1) return DSA_ERR_SHAPE;
   }
+  if (out_bytes < dsa_gather_dequant_workspace_bytes(T, K, pool_rows, layout)) return DSA_ERR_WORKSPACE;
   if (!aligned(pool_dev, 16) || !aligned(out_bf16_dev, 16) || !aligned(topk_dev, 4) ||
       !aligned(idx_out_dev, 4))
     return DSA_ERR_ALIGN;
@@ -213,7 +234,8 @@ int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
   dsa::GatherArgs g{};
   g.pool = static_cast<const uint8_t*>(pool_dev);
   g.pool_rows = pool_rows;
-  g.scaled = layout == DSA_KV_SCALED528;
+  g.layout = layout;
+  g.full_pool = !((int64_t)T * K < pool_rows);
   g.page_table = page_table_dev;
   g.B = B;
   g.max_pages = max_pages;
@@ -233,7 +255,10 @@ int dsa_gather_dequant(const void* pool_dev, int64_t pool_rows, int layout,
 size_t dsa_sparse_attn_workspace_bytes(int T, int H, int K) {
   int sms = 0;
   if (current_device_sms(&sms) != DSA_OK) sms = 152;
-  return dsa::plan_attn(T, H, K, sms).ws_bytes;
+  // enough for every layout: 656-byte rows use head groups of at most 16
+  const size_t a = dsa::plan_attn(T, H, K, sms, false).ws_bytes;
+  const size_t b = dsa::plan_attn(T, H, K, sms, true).ws_bytes;
+  return a > b ? a : b;
 }
 
 int dsa_sparse_attn_decode(const void* q_bf16_dev, int T, int H, int D, const void* pool_dev,

@@ -41,6 +41,7 @@ struct AttnArgs {
   float* ws_o;            // [grid][2][hg][512] normalised partial O (slot 0: the CTA's first unit)
   float* ws_lse;          // [grid][2][hg]
   int32_t* err;
+  uint64_t wait_ns;       // limit of every bounded wait inside the kernel
 };
 
 // Launch plan shared by the workspace query and the launch.  Workspace (only
@@ -53,7 +54,7 @@ struct AttnPlan {
   size_t ws_o_offset, ws_lse_offset;
   size_t ws_bytes;
 };
-AttnPlan plan_attn(int T, int H, int K, int sms);
+AttnPlan plan_attn(int T, int H, int K, int sms, bool rope);
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
 
@@ -61,24 +62,32 @@ void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
 struct GatherArgs {
   const uint8_t* pool;
   int64_t pool_rows;
-  bool scaled;            // 528-byte (or 656-byte) rows: group scales
-  bool rope;              // 656-byte rows: 64 BF16 RoPE dims after the scales
+  int layout;             // DSA_KV_RAW512, DSA_KV_SCALED528 or DSA_KV_ROPE656
+  bool full_pool;         // T*K >= pool_rows: dequantise the whole pool
   const int32_t* page_table;
   int B, max_pages, page_size;
   const int32_t* token_seq;
   const int32_t* topk;    // [T, K]
   int T, K;
-  void* out;              // BF16 [T*K, 512]
+  void* out;              // BF16 [gather_rows(pool_rows, T*K), 512 or 576]
   int32_t* idx_out;       // [T, K]
   int32_t* err;
 };
+// Rows of the reader's workspace: min(pool_rows, selected entries).
+int64_t gather_rows(int64_t pool_rows, int64_t n_selected);
 void launch_gather_dequant(const GatherArgs& g, int sms, cudaStream_t stream);
 
 // Merges the partial results of split units (after the attention kernel).
 void launch_combine(const AttnArgs& a, cudaStream_t stream);
 
-// Heads handled together by one CTA of the attention kernel.
-int head_group(int H);
+// DSA_OK and the SM count when the current device has compute capability
+// 10.3, else DSA_ERR_DEVICE.
+int current_device_sms(int* sms);
+
+// Heads handled together by one CTA of the attention kernel: up to 32, up to
+// 16 over 656-byte rows (whose RoPE operands take the shared memory of the
+// larger groups).
+int head_group(int H, bool rope);
 
 // The persistent schedule: CTA c owns global tiles [tile_begin(c), tile_begin(c + 1)).
 __host__ __device__ __forceinline__ int64_t tile_begin(int c, int64_t n_tiles, int grid) {

@@ -26,12 +26,24 @@ __device__ __forceinline__ void load_row16(const uint16_t* __restrict__ row, int
   }
 }
 
+// Four floats -> four E4M3 bytes (saturating round-to-nearest-even); a NaN
+// input gives the FN NaN code 0x7F with the input's sign bit (the cvt
+// instruction alone returns 0x7F for NaN of either sign).
+__device__ __forceinline__ uint32_t e4m3x4_keep_nan_sign(float a, float b, float c, float d) {
+  uint32_t r = e4m3x4_satrne(a, b, c, d);
+  const float v[4] = {a, b, c, d};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (v[i] != v[i]) r = (r & ~(0xFFu << (8 * i))) | ((0x7Fu | ((__float_as_uint(v[i]) >> 31) << 7)) << (8 * i));
+  return r;
+}
+
 __device__ __forceinline__ void store_row16(uint8_t* __restrict__ row, int lane, const Row16& r) {
   uint2 lo, hi;
-  lo.x = e4m3x4_satrne(r.v[0], r.v[1], r.v[2], r.v[3]);
-  lo.y = e4m3x4_satrne(r.v[4], r.v[5], r.v[6], r.v[7]);
-  hi.x = e4m3x4_satrne(r.v[8], r.v[9], r.v[10], r.v[11]);
-  hi.y = e4m3x4_satrne(r.v[12], r.v[13], r.v[14], r.v[15]);
+  lo.x = e4m3x4_keep_nan_sign(r.v[0], r.v[1], r.v[2], r.v[3]);
+  lo.y = e4m3x4_keep_nan_sign(r.v[4], r.v[5], r.v[6], r.v[7]);
+  hi.x = e4m3x4_keep_nan_sign(r.v[8], r.v[9], r.v[10], r.v[11]);
+  hi.y = e4m3x4_keep_nan_sign(r.v[12], r.v[13], r.v[14], r.v[15]);
   reinterpret_cast<uint2*>(row)[lane] = lo;
   reinterpret_cast<uint2*>(row + 256)[lane] = hi;
 }
@@ -106,10 +118,11 @@ __global__ void __launch_bounds__(256, 4) kv_write_scaled_kernel(
     }
     const float s0 = a0 == 0.f ? 0.f : __fdiv_rn(a0, 448.0f);
     const float s1 = a1 == 0.f ? 0.f : __fdiv_rn(a1, 448.0f);
+    // copysignf: the same quotient (s > 0), and a NaN keeps its input's sign
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      r.v[k] = s0 == 0.f ? 0.f : __fdiv_rn(r.v[k], s0);
-      r.v[8 + k] = s1 == 0.f ? 0.f : __fdiv_rn(r.v[8 + k], s1);
+      r.v[k] = s0 == 0.f ? 0.f : copysignf(__fdiv_rn(r.v[k], s0), r.v[k]);
+      r.v[8 + k] = s1 == 0.f ? 0.f : copysignf(__fdiv_rn(r.v[8 + k], s1), r.v[8 + k]);
     }
     uint8_t* row = pool + s * kRowBytes;
     store_row16(row, lane, r);
@@ -151,7 +164,7 @@ __global__ void __launch_bounds__(256, 4) quantize_q8_kernel(
     a = warp_max(a);
     const float s = a == 0.f ? 0.f : __fdiv_rn(a, 448.0f);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) r.v[k] = s == 0.f ? 0.f : __fdiv_rn(r.v[k], s);
+    for (int k = 0; k < 16; ++k) r.v[k] = s == 0.f ? 0.f : copysignf(__fdiv_rn(r.v[k], s), r.v[k]);
     store_row16(q8 + i * kD, lane, r);
     if (lane == 0) scale[i] = s;
   };

@@ -10,13 +10,16 @@
 //
 // The array's address is looked up once per device (cudaGetSymbolAddress,
 // with that device current) on the first call made on that device; the host
-// symbol itself is only a stand-in and is never handed to a kernel.
+// symbol itself is only a stand-in and is never handed to a kernel.  The
+// address stays cached for the life of the process: a cudaDeviceReset, which
+// unloads the module and may place the array elsewhere, invalidates it.
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/dsa.h"
+#include "kernels.h"
 
 namespace {
 
@@ -67,8 +70,17 @@ extern "C" int dsa_sparse_attn_decode_noalloc(const void* q_bf16_dev, int T, int
   const int width = layout == DSA_KV_ROPE656 ? 576 : 512;
   if (D != width || kv_row_dim != width) return DSA_ERR_ROW_WIDTH;
   if (K <= 0 || K % 128 != 0) return DSA_ERR_TOPK_PAD;
-  if (!heads_supported(H) || (layout == DSA_KV_ROPE656 && H > 16)) return DSA_ERR_HEADS;
+  if (!heads_supported(H)) return DSA_ERR_HEADS;
   if (T == 0) return DSA_OK;
+  int sms = 0;
+  if (dsa::current_device_sms(&sms) != DSA_OK) {
+    // no usable device: the decode entry point's own checks give the status
+    // (an argument error if there is one, else DSA_ERR_DEVICE); it launches
+    // nothing on this path
+    return dsa_sparse_attn_decode(q_bf16_dev, T, H, D, pool_dev, pool_rows, layout, kv_row_dim,
+                                  page_table_dev, B, max_pages, page_size, token_seq_dev, topk_dev, K,
+                                  sm_scale, o_bf16_dev, lse_dev, nullptr, 0, err_flag_dev, stream);
+  }
   if (dsa_sparse_attn_workspace_bytes(T, H, K) > kScratchBytes) return DSA_ERR_WORKSPACE;
   void* ws = nullptr;
   const int st = scratch_on_current_device(&ws);

@@ -6,10 +6,10 @@
 
 namespace dsa {
 // One persistent CTA per SM (fewer when there are fewer tiles than SMs).
-AttnPlan plan_attn(int T, int H, int K, int sms) {
+AttnPlan plan_attn(int T, int H, int K, int sms, bool rope) {
   AttnPlan p{};
   if (T <= 0 || H <= 0 || K <= 0 || sms <= 0) return p;
-  p.hg = head_group(H);
+  p.hg = head_group(H, rope);
   p.hgs = H / p.hg;
   p.tpt = (K + 127) / 128;
   p.n_tiles = (int64_t)T * p.hgs * p.tpt;

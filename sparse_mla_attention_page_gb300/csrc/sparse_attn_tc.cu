@@ -209,8 +209,23 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t v16) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-__device__ __forceinline__ void st_shared_u8(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Byte offset of P column n (query column: head x term), tile row k in the
+// PV B operand: MN-major without swizzle, core matrices of 8 rows x 16
+// columns (128 bytes); the NP / 16 core matrices of one 8-row group are
+// adjacent, so groups of 8 rows lie NP * 8 bytes apart.
+template <int NP>
+__device__ __forceinline__ uint32_t p_off(int n, int k) {
+  return (n >> 4) * 128 + (k >> 3) * (NP * 8) + (k & 7) * 16 + (n & 15);
 }
 
 // 16-byte copy; bytes beyond src_bytes (0 or 16) are zero-filled and not read.
@@ -233,8 +248,8 @@ __device__ __forceinline__ float scale_pow2(float x, int e) {
 }
 
 // Warp-uniform bounded wait (all lanes agree on the outcome).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -445,7 +460,7 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
     // publish the rows first: the producers wait for them, nothing here waits
     // for the loads of later tiles still in flight
     const int slot = it % kRing;
-    if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort)) break;
+    if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort, a.wait_ns)) break;
     *reinterpret_cast<int4*>(&ms.ring[slot][4 * lane]) = make_int4(rows[0], rows[1], rows[2], rows[3]);
     mbar_arrive(smem_u32(&ms.idx_full[slot]));
     // entries of tile it + 1 + kAhead; page-table reads of tile it + 1
@@ -476,8 +491,8 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
   const uint32_t kv0 = smem_u32(sm + C::KV_OFF);
   for (int it = 0; it < n_it; ++it) {
     const int stage = it % C::NST, slot = it % kRing;
-    if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort)) break;
-    if (!warp_wait(smem_u32(&ms.idx_full[slot]), (it / kRing) & 1, abort)) break;
+    if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort, a.wait_ns)) break;
+    if (!warp_wait(smem_u32(&ms.idx_full[slot]), (it / kRing) & 1, abort, a.wait_ns)) break;
     int32_t rows[kRowsPerWarp / 4];
 #pragma unroll
     for (int g = 0; g < kRowsPerWarp / 4; ++g) rows[g] = ms.ring[slot][kRowsPerWarp * pw + 4 * g + rq];
@@ -536,7 +551,7 @@ __device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem
   const uint32_t q0 = smem_u32(sm + C::Q_OFF);
   const uint32_t p0 = smem_u32(sm + C::P_OFF);
   constexpr uint32_t kIdQK = idesc_e4m3(C::NQ, false);
-  constexpr uint32_t kIdPV = idesc_e4m3(C::NP, true);
+  constexpr uint32_t kIdPV = idesc_e4m3(C::NP, true, true);
   constexpr uint32_t kIdRope = idesc_bf16(C::NR > 0 ? C::NR : 16);
   const uint32_t rope0 = smem_u32(sm + C::ROPE_OFF);
   const uint32_t qr0 = smem_u32(sm + C::QR_OFF);
@@ -560,7 +575,9 @@ __device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem
 #pragma unroll
           for (int js = 0; js < 4; ++js) {
             const uint64_t ad = sdesc_sw128(a_base + db * 16384 + js * 4096, 1024, 1024);
-            const uint64_t bd = sdesc_sw128(b_base + (kScaled ? db * (C::NP * 128) : 0) + js * 32, 16, 1024);
+            // rows 32 js .. 32 js + 31 of P: four groups of 8 rows
+            const uint64_t bd = sdesc_mn_none(b_base + (kScaled ? db * (C::NP * 128) : 0) + js * 4 * (C::NP * 8),
+                                              C::NP * 8, 128);
             mma_e4m3(tmem + C::O_COL0 + db * C::NP, ad, bd, kIdPV, (!pv_first || js > 0) ? 1u : 0u);
           }
         }
@@ -624,7 +641,7 @@ __device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem
       idle_since = globaltimer_ns();
     } else if (*abort) {
       break;
-    } else if (globaltimer_ns() - idle_since > 1000000000ull) {
+    } else if (globaltimer_ns() - idle_since > a.wait_ns) {
       *abort = 1;
       break;
     }
@@ -695,7 +712,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     if (first) {
       ++seg;
       const int qb = seg % C::NQB;
-      ok &= mbar_wait(smem_u32(&ms.q_full[qb]), (seg / C::NQB) & 1, abort);
+      ok &= mbar_wait(smem_u32(&ms.q_full[qb]), (seg / C::NQB) & 1, abort, a.wait_ns);
       m_lane = -INFINITY;
 #pragma unroll
       for (int h = 0; h < HPT; ++h) {
@@ -706,11 +723,11 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       for (int g = 0; g < 4; ++g) e_grp[g] = -1000;
     }
     const int qb = seg % C::NQB;
-    ok &= mbar_wait(smem_u32(&ms.meta_full[stage]), (it / C::NST) & 1, abort);
+    ok &= mbar_wait(smem_u32(&ms.meta_full[stage]), (it / C::NST) & 1, abort, a.wait_ns);
     const bool valid = (ms.vmask[stage][row & 3] >> (row >> 2)) & 1u;
     float sc4[4] = {1.f, 1.f, 1.f, 1.f};
     if (kScaled) {
-      ok &= mbar_wait(smem_u32(&ms.kv_full[stage]), (it / C::NST) & 1, abort);
+      ok &= mbar_wait(smem_u32(&ms.kv_full[stage]), (it / C::NST) & 1, abort, a.wait_ns);
       const float4 v = *reinterpret_cast<const float4*>(sm + C::SC_OFF + stage * kScStage + row * 16);
       sc4[0] = v.x; sc4[1] = v.y; sc4[2] = v.z; sc4[3] = v.w;
     }
@@ -720,7 +737,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
     for (int qc = 0; qc < C::NQC; ++qc) {
       const int u = it * C::NQC + qc, sb = u % C::NS;
-      ok &= mbar_wait(smem_u32(&ms.s_full[sb]), (u / C::NS) & 1, abort);
+      ok &= mbar_wait(smem_u32(&ms.s_full[sb]), (u / C::NS) & 1, abort, a.wait_ns);
       tc_fence_after();
 #pragma unroll
       for (int gl = 0; gl < C::GC; ++gl) {
@@ -823,7 +840,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       float alpha[HPT];
 #pragma unroll
       for (int h = 0; h < HPT; ++h) alpha[h] = __shfl_sync(0xffffffffu, alpha_lane, h);
-      ok &= mbar_wait(smem_u32(&ms.pv_done[(it - 1) % C::NPB]), ((it - 1) / C::NPB) & 1, abort);
+      ok &= mbar_wait(smem_u32(&ms.pv_done[(it - 1) % C::NPB]), ((it - 1) / C::NPB) & 1, abort, a.wait_ns);
       tc_fence_after();
 #pragma unroll
       for (int db = 0; db < 4; ++db) {
@@ -843,7 +860,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     // this P buffer was last read by PV(it - NPB); with a single buffer the
     // wait comes after P is formed in registers, just before it is stored
     constexpr bool kLateWait = C::NPB == 1 && C::G == 1;
-    if (!kLateWait && it >= C::NPB) ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), ((it / C::NPB) - 1) & 1, abort);
+    if (!kLateWait && it >= C::NPB) ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), ((it / C::NPB) - 1) & 1, abort, a.wait_ns);
     const uint32_t pbuf = smem_u32(sm + C::P_OFF + pb * C::P_BYTES);
     // p = 2^(s - m) (0 while the head has seen no valid entry), denominators, P operand
 #pragma unroll
@@ -860,32 +877,36 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       const float2 mf = e4m3x2_to_f32x2(mid2);
       lo2 = e4m3x2_satrne((r0 - mf.x) * 16.f, (r1 - mf.y) * 16.f);
     };
-    auto store = [&](uint32_t pg, int n, uint32_t hi2, uint32_t mid2, uint32_t lo2) {
-      st_shared_u8(pg + kmajor_off<C::NP>(n, row), hi2 & 0xFFu);
-      st_shared_u8(pg + kmajor_off<C::NP>(n + 1, row), (hi2 >> 8) & 0xFFu);
-      st_shared_u8(pg + kmajor_off<C::NP>(HG + n, row), mid2 & 0xFFu);
-      st_shared_u8(pg + kmajor_off<C::NP>(HG + n + 1, row), (mid2 >> 8) & 0xFFu);
-      st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n, row), lo2 & 0xFFu);
-      st_shared_u8(pg + kmajor_off<C::NP>(2 * HG + n + 1, row), (lo2 >> 8) & 0xFFu);
+    // one term's HPT bytes of this row (P columns term * HG + hbase ..) in one
+    // store: they are consecutive in the MN-major operand
+    auto store_term = [&](uint32_t pg, int term, const uint32_t (&t2)[HPT / 2]) {
+      const uint32_t addr = pg + p_off<C::NP>(term * HG + hbase, row);
+      if constexpr (HPT == 16)
+        st_shared_v4(addr, t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16), t2[4] | (t2[5] << 16), t2[6] | (t2[7] << 16));
+      else if constexpr (HPT == 8)
+        st_shared_v2(addr, t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16));
+      else
+        st_shared_u32(addr, t2[0] | (t2[1] << 16));
     };
     if constexpr (kLateWait) {
       uint32_t hi2[HPT / 2], mid2[HPT / 2], lo2[HPT / 2];
 #pragma unroll
       for (int h = 0; h < HPT; h += 2) split(s2[h], s2[h + 1], hi2[h / 2], mid2[h / 2], lo2[h / 2]);
-      if (it >= 1) ok &= mbar_wait(smem_u32(&ms.pv_done[0]), (it - 1) & 1, abort);
-#pragma unroll
-      for (int h = 0; h < HPT; h += 2) store(pbuf, hbase + h, hi2[h / 2], mid2[h / 2], lo2[h / 2]);
+      if (it >= 1) ok &= mbar_wait(smem_u32(&ms.pv_done[0]), (it - 1) & 1, abort, a.wait_ns);
+      store_term(pbuf, 0, hi2);
+      store_term(pbuf, 1, mid2);
+      store_term(pbuf, 2, lo2);
     } else {
 #pragma unroll
       for (int g = 0; g < C::G; ++g) {
         const float mul = kScaled ? (e_grp[g] == -1000 ? 0.f : scale_pow2(sc4[g], -e_grp[g])) : 1.f;
         const uint32_t pg = pbuf + g * (C::NP * 128);
+        uint32_t hi2[HPT / 2], mid2[HPT / 2], lo2[HPT / 2];
 #pragma unroll
-        for (int h = 0; h < HPT; h += 2) {
-          uint32_t hi2, mid2, lo2;
-          split(s2[h] * mul, s2[h + 1] * mul, hi2, mid2, lo2);
-          store(pg, hbase + h, hi2, mid2, lo2);
-        }
+        for (int h = 0; h < HPT; h += 2) split(s2[h] * mul, s2[h + 1] * mul, hi2[h / 2], mid2[h / 2], lo2[h / 2]);
+        store_term(pg, 0, hi2);
+        store_term(pg, 1, mid2);
+        store_term(pg, 2, lo2);
       }
     }
     fence_proxy_async_smem();
@@ -913,7 +934,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       ms.lse2[hbase + lane] = l > 0.f ? m_lane + log2f(l) : -INFINITY;
     }
     named_bar_sync(1, kSmxThreads);
-    ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), (it / C::NPB) & 1, abort);
+    ok &= mbar_wait(smem_u32(&ms.pv_done[pb]), (it / C::NPB) & 1, abort, a.wait_ns);
     tc_fence_after();
     const int64_t u0 = cur.unit * a.tpt;
     const int h0 = cur.hgi * a.hg;
@@ -1059,7 +1080,7 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
 template <int HG>
 void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
   if (a.rope) {
-    if constexpr (HG <= 16) launch_tc<HG, true, false, true>(a, stream);   // host checks H
+    if constexpr (HG <= 16) launch_tc<HG, true, false, true>(a, stream);   // head_group caps HG at 16
   } else if (q8 && a.scaled) {
     launch_tc<HG, true, true, false>(a, stream);
   } else if (q8) {
@@ -1074,7 +1095,10 @@ void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
 
 }  // namespace
 
-int head_group(int H) { return H < 32 ? H : 32; }
+int head_group(int H, bool rope) {
+  const int cap = rope ? 16 : 32;
+  return H < cap ? H : cap;
+}
 
 void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream) {
   if (a.hg == 8) launch_hg<8>(a, q8, stream);

@@ -57,19 +57,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Arrive once on `bar` and add `bytes` to the transaction count it waits for.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Bulk (TMA, 1-D) copy global -> shared of `bytes` (multiple of 16, both
-// addresses 16-byte aligned); completes `bytes` transactions on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -80,11 +67,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-// 16-byte global -> shared copy, L2 only (no L1 allocation).
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // The mbarrier receives one arrival once all prior cp.async of this thread are complete.
@@ -156,11 +138,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor without swizzle (layout type 0) for an
+// MN-major operand: core matrices of 8 K-rows x 16 bytes (16 consecutive
+// MN elements of one K index per 16-byte row), `kstride` bytes between
+// groups of 8 K-rows (leading byte offset) and `mnstride` bytes between
+// groups of 16 MN elements (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_mn_none(uint32_t addr, uint32_t kstride, uint32_t mnstride) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((kstride >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((mnstride >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // Instruction descriptor for kind::f8f6f4: D = F32, A = B = E4M3, M = 128,
-// A K-major or MN-major, B K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int n, bool a_mn_major) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(n >> 3) << 17) |
-         ((128u >> 4) << 24);
+// each of A and B K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int n, bool a_mn_major, bool b_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -194,17 +186,8 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// 32 lanes x 32-bit, 16 consecutive columns: thread i of the warp gets lane
-// (warp quarter base + i), columns [col, col+16).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15])
-      : "r"(taddr));
-}
-
+// 32 lanes x 32-bit, 8 consecutive columns: thread i of the warp gets lane
+// (warp quarter base + i), columns [col, col+8).
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
@@ -233,15 +216,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {

@@ -66,17 +66,32 @@ def run_prefill(w: dict, pool_d: torch.Tensor, q8: np.ndarray, q_scale: np.ndarr
             int(err_d.item()))
 
 
+def attn_error_stats(O, L, Or, Lr) -> dict:
+    """max |O - O_ref|, the same relative to max |O_ref| (how large the error is
+    next to the output itself), and max |LSE - LSE_ref| where finite."""
+    d = np.abs(O - Or)
+    scale = float(np.abs(Or).max()) if Or.size else 0.0
+    neg = np.isneginf(Lr)
+    dl = np.abs(L[~neg] - Lr[~neg])
+    return {"max_abs": float(d.max()) if d.size else 0.0,
+            "rel_to_max": float(d.max() / scale) if d.size and scale > 0 else 0.0,
+            "max_ref": scale, "lse_max_abs": float(dl.max()) if dl.size else 0.0}
+
+
 def assert_attn_close(O, L, Or, Lr, what=""):
-    """Elementwise tolerance check with a readable report of the worst offender."""
+    """Elementwise tolerance check with a readable report of the worst offender
+    and of the error relative to max |O_ref|; returns the error statistics."""
     assert O.shape == Or.shape and L.shape == Lr.shape
+    st = attn_error_stats(O, L, Or, Lr) if np.isfinite(O).all() else {}
     excess = np.abs(O - Or) - (O_ATOL + O_RTOL * np.abs(Or))
     if (excess > 0).any() or not np.isfinite(O).all():
         i = np.unravel_index(np.nanargmax(np.where(np.isfinite(excess), excess, np.inf)), excess.shape)
         raise AssertionError(f"{what} O mismatch at {i}: got {O[i]} ref {Or[i]} "
-                             f"({int((excess > 0).sum())} elements out of tolerance)")
+                             f"({int((excess > 0).sum())} elements out of tolerance; {st})")
     neg = np.isneginf(Lr)
     assert np.array_equal(np.isneginf(L), neg), f"{what} LSE -inf pattern differs"
     d = np.abs(L[~neg] - Lr[~neg])
     if d.size and d.max() > LSE_ATOL:
         i = np.argmax(d)
-        raise AssertionError(f"{what} LSE mismatch: max |diff| {d.max()} (got {L[~neg][i]} ref {Lr[~neg][i]})")
+        raise AssertionError(f"{what} LSE mismatch: max |diff| {d.max()} (got {L[~neg][i]} ref {Lr[~neg][i]}; {st})")
+    return st

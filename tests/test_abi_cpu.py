@@ -70,7 +70,7 @@ def prefill(L, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(D=576), 4), (dict(kvd=528), 4), (dict(layout=3), 3), (dict(layout=2), 4),
-    (dict(layout=2, D=576, kvd=576, H=32), 6), (dict(K=0), 5), (dict(K=2000), 5),
+    (dict(layout=2, D=576, kvd=576, H=24), 6), (dict(K=0), 5), (dict(K=2000), 5),
     (dict(H=12), 6), (dict(H=256), 6), (dict(T=-1), 2), (dict(q=None), 1), (dict(pool=None), 1),
     (dict(topk=None), 1), (dict(o=None), 1), (dict(lse=None), 1), (dict(rows=0), 2),
     (dict(pt=FAKE, B=0), 2), (dict(pt=FAKE, ps=0), 2), (dict(q=FAKE + 8), 10), (dict(o=FAKE + 4), 10),
@@ -89,10 +89,10 @@ def test_prefill_host_validation(L, kw, code):
 
 def gather(L, **kw):
     a = dict(pool=FAKE, rows=4096, layout=0, pt=None, B=1, mp=64, ps=64, ts=None, topk=FAKE, T=4, K=100,
-             out=FAKE, idx=FAKE, err=None)
+             out=FAKE, ob=1 << 30, idx=FAKE, err=None)
     a.update(kw)
     return L.dsa_gather_dequant(a["pool"], a["rows"], a["layout"], a["pt"], a["B"], a["mp"], a["ps"], a["ts"],
-                                a["topk"], a["T"], a["K"], a["out"], a["idx"], a["err"], None)
+                                a["topk"], a["T"], a["K"], a["out"], a["ob"], a["idx"], a["err"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -100,9 +100,23 @@ def gather(L, **kw):
     (dict(topk=None), 1), (dict(out=None), 1), (dict(idx=None), 1), (dict(rows=0), 2),
     (dict(T=1 << 20, K=4096), 2), (dict(pt=FAKE, B=0), 2), (dict(pool=FAKE + 4), 10),
     (dict(out=FAKE + 8), 10), (dict(topk=FAKE + 2), 10),
+    (dict(ob=400 * 1024 - 1), 7), (dict(layout=2, ob=400 * 1152 - 2), 7),
+    (dict(T=64, K=2048, rows=131072, ob=131072 * 1024 - 1), 7),
 ])
 def test_gather_host_validation(L, kw, code):
     assert gather(L, **kw) == code
+
+
+def test_gather_workspace_bytes(L):
+    """min(pool rows, selected entries) rows of 1024 bytes (1152 for 656-byte rows)."""
+    f = L.dsa_gather_dequant_workspace_bytes
+    assert f(4, 100, 4096, 0) == 400 * 1024
+    assert f(4, 100, 4096, 1) == 400 * 1024
+    assert f(4, 100, 4096, 2) == 400 * 1152
+    assert f(64, 2048, 131072, 0) == 131072 * 1024          # T*K == pool rows: the full pool
+    assert f(128, 2048, 131072, 1) == 131072 * 1024
+    assert f(4096, 2048, 16384, 0) == 16384 * 1024
+    assert f(1, 1, 10, 7) == 0 and f(-1, 4, 10, 0) == 0
 
 
 def test_writer_host_validation(L):

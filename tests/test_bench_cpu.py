@@ -46,10 +46,40 @@ def test_algorithmic_bytes_prefill_and_rope():
 
 
 def test_defaults(monkeypatch):
+    """The headline is the largest single-GPU batch (the Q8 prefill); at least
+    3 warm-up steps; every per_config entry names a known workload or op."""
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse_args()
-    assert (a.gpus, a.impl, a.workload, a.op) == (1, "ours", "decode_raw512", "attention")
-    assert a.warmup >= 3 and a.steps >= 1 and not a.warm
+    assert (a.gpus, a.impl, a.workload) == (1, "ours", "prefill_q8_raw512")
+    assert a.warmup >= 3 and a.steps >= 1 and not a.warm and not a.no_per_config
+    keys = [k for k, _, _, _ in bench.PER_CONFIG]
+    assert len(keys) == len(set(keys))
+    for key, kind, wname, opt in bench.PER_CONFIG:
+        assert kind in ("attention", "kv_write", "gather_dequant")
+        assert wname is None or wname in W.WORKLOADS
+        assert kind != "kv_write" or opt["layout"] in bench.ROW_BYTES
+    for need in ("tiny_decode_raw512", "decode_raw512", "decode_scaled528", "kv_write_raw512",
+                 "kv_write_scaled528", "writer_sweep_raw512_h32", "writer_sweep_scaled528_h8"):
+        assert need in keys
+
+
+def test_gather_and_writer_bytes():
+    """The reader moves each valid entry's row and BF16 output row when entries
+    are fewer than pool rows, else the whole pool once; plus the lists."""
+    w = W.tiny_decode_raw512()
+    v = int((w["topk"] >= 0).sum())
+    assert bench.gather_bytes(w) == v * (512 + 1024) + w["T"] * w["K"] * 8
+    w2 = W.decode_raw512(T=8, K=256, pool_rows=2048)
+    assert w2["T"] * w2["K"] >= w2["pool_rows"]
+    assert bench.gather_bytes(w2) == 2048 * (512 + 1024) + 8 * 256 * 8
+    assert bench.writer_bytes(10, "scaled528") == 10 * (1024 + 528 + 8)
+    assert bench.writer_bytes(10, "rope656") == 10 * (1152 + 656 + 8)
+
+
+def test_tensor_peak_choice():
+    assert bench.tensor_peak({"bf16_tflops": 1000.0}, {"tflops": 3500.0}) == (3500.0, "measured FP8 burst")
+    assert bench.tensor_peak({"bf16_tflops": 1000.0}, {"tflops": None})[0] == 2000.0
+    assert bench.tensor_peak({}, None)[0] == 2 * bench.FALLBACK_BF16_TFLOPS
 
 
 def test_reference_arm_line():

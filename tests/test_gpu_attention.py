@@ -121,10 +121,13 @@ def test_prefill_q8_scaled528(T, full):
     assert_attn_close(O, L, Or, Lr, f"prefill_q8_scaled528 T={T}")
 
 
-@pytest.mark.parametrize("T,K,H,full", [(16, 512, 16, True), (8, 256, 8, True), (64, 2048, 16, False)])
+@pytest.mark.parametrize("T,K,H,full", [(16, 512, 16, True), (8, 256, 8, True), (64, 2048, 16, False),
+                                         (12, 384, 32, True), (5, 256, 64, True), (2, 256, 128, True),
+                                         (64, 2048, 32, False)])
 def test_decode_rope656(T, K, H, full):
     """656-byte rows: group-scaled latent plus 64 BF16 RoPE dims; 576-wide
-    queries and keys (the RoPE scores by BF16 MMAs), 512-wide values."""
+    queries and keys (the RoPE scores by BF16 MMAs), 512-wide values; 32 and
+    more heads run as head groups of 16."""
     w = W.decode_rope656(T=T, K=K, H=H, pool_rows=131072 if not full else 16384)
     pool, pd = pool_for(w, ("rope", T, K, H))
     O, L, err = run_decode(w, pd)
@@ -134,6 +137,37 @@ def test_decode_rope656(T, K, H, full):
     if tok is not None:
         O, L = O[tok], L[tok]
     assert_attn_close(O, L, Or, Lr, f"decode_rope656 T={T} H={H}")
+
+
+@pytest.mark.parametrize("layout", ["raw512", "scaled528", "rope656", "q8_raw512"])
+def test_peaked_softmax(layout):
+    """Queries scaled up (x100) so each head's logits spread over far more than
+    2^8 in log2 units and a handful of entries carry the softmax: O is then
+    about the size of a KV row, so the tolerance sees errors in PV, and the
+    running maximum is raised mid-segment (the O rescale path).  Besides the
+    elementwise tolerance, the largest error must stay within 1 % of max |O|."""
+    T, H, K = 8, 16, 1024
+    if layout == "rope656":
+        w = W.decode_rope656(seed=300, T=T, H=H, K=K, pool_rows=8192)
+    elif layout == "scaled528":
+        w = W.decode_scaled528(seed=301, T=T, H=H, K=K, pool_rows=8192)
+    else:
+        w = W.decode_raw512(seed=302, T=T, H=H, K=K, pool_rows=8192, special_tokens=False)
+    q = W.bf16_bits_to_f32(w["q_bf16"]) * np.float32(100.0)
+    w["q_bf16"] = W.f32_to_bf16_bits(q)
+    pool, pd = pool_for(w, ("peaked", layout))
+    if layout == "q8_raw512":
+        q8, qs = oracle.quantize_q8(w["q_bf16"])
+        O, L, err = run_prefill(w, pd, q8, qs)
+        Or, Lr, _ = oracle.sparse_attn(pool, "raw512", w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                                       page_table=w["page_table"])
+    else:
+        O, L, err = run_decode(w, pd)
+        Or, Lr, _ = oracle_decode(w, pool)
+    assert err == 0
+    st = assert_attn_close(O, L, Or, Lr, f"peaked {layout}")
+    assert st["max_ref"] > 0.3, st                         # O is row-sized, not ~0.01
+    assert st["rel_to_max"] <= 1e-2, st
 
 
 def test_prefill_q8_short_context_padding():

@@ -30,8 +30,9 @@ def _write_gpu(layout, x_bits, slots, pool_init):
 
 @pytest.mark.parametrize("layout", ["raw512", "scaled528"])
 def test_every_bf16_input_bit_exact(layout):
-    """Every BF16 bit pattern (NaN excluded; inf too for the scaled layout),
-    shuffled into rows so that groups mix magnitudes."""
+    """Every BF16 bit pattern (NaN patterns have their own test; inf is
+    excluded for the scaled layout, where it turns the group's scale into
+    inf), shuffled into rows so that groups mix magnitudes."""
     bits = _finite_bf16_patterns(include_inf=(layout == "raw512"))
     rng = np.random.default_rng(100)
     bits = bits[rng.permutation(bits.size)]
@@ -47,6 +48,53 @@ def test_every_bf16_input_bit_exact(layout):
     assert err == 0
     bad = np.argwhere(got != ref)
     assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:3].tolist()}"
+
+
+def _nan_bf16_patterns() -> np.ndarray:
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    return bits[np.isnan(W.bf16_bits_to_f32(bits))]
+
+
+@pytest.mark.parametrize("layout", ["raw512", "scaled528", "rope656"])
+def test_nan_inputs_bit_exact(layout):
+    """Every BF16 NaN pattern (both signs, all payloads), scattered among
+    finite values: the NaN encodes as 0x7F with the input's sign, and the
+    group scales ignore it (they are taken over the finite values)."""
+    nan = _nan_bf16_patterns()
+    assert nan.size == 254
+    rng = np.random.default_rng(101)
+    width = 576 if layout == "rope656" else 512
+    n = 32
+    x = W.f32_to_bf16_bits((rng.standard_normal((n, width)) * rng.uniform(0.1, 8, (n, 1))).astype(np.float32))
+    pos = rng.choice(n * 512, nan.size, replace=False)            # latent dims only
+    flat = x[:, :512].reshape(-1).copy()
+    flat[pos] = nan
+    x[:, :512] = flat.reshape(n, 512)
+    slots = rng.permutation(n + 5)[:n].astype(np.int64)
+    init = np.full((n + 5, oracle.row_bytes(layout)), 0x3C, dtype=np.uint8)
+    ref = init.copy()
+    oracle.kv_write(layout, x, slots, ref)
+    got, err = _write_gpu(layout, x, slots, init)
+    assert err == 0
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:3].tolist()}: got {got[tuple(bad[0])]:#x} want {ref[tuple(bad[0])]:#x}"
+
+
+def test_quantizer_nan_inputs_bit_exact():
+    """The FP8 query quantiser over vectors holding every BF16 NaN pattern."""
+    nan = _nan_bf16_patterns()
+    rng = np.random.default_rng(102)
+    q = W.f32_to_bf16_bits(rng.standard_normal((8, 4, 512)).astype(np.float32))
+    flat = q.reshape(-1).copy()
+    flat[rng.choice(flat.size, nan.size, replace=False)] = nan
+    q = flat.reshape(q.shape)
+    q8r, qsr = oracle.quantize_q8(q)
+    q8 = torch.empty(8, 4, 512, dtype=torch.uint8, device="cuda")
+    qs = torch.empty(8, 4, dtype=torch.float32, device="cuda")
+    binding.dsa_quantize_q8(bf16_dev(q), q8, qs)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(q8.cpu().numpy(), q8r)
+    np.testing.assert_array_equal(qs.cpu().numpy().view(np.uint32), qsr.view(np.uint32))
 
 
 @pytest.mark.parametrize("layout", ["raw512", "scaled528"])
