@@ -80,11 +80,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSmxWarps = 8;        // softmax warps: warp w -> lane quarter w % 4, head half w / 4
 constexpr int kSmxThreads = kSmxWarps * 32;
-constexpr int kMmaWarp = 8;
-constexpr int kIdxWarp = 9;
-constexpr int kProdWarp0 = 10;
-constexpr int kProdWarps = 2;
-constexpr int kThreads = 32 * (kSmxWarps + 2 + kProdWarps);
+constexpr int kQkWarp = 8;          // issues QK^T
+constexpr int kPvWarp = 9;          // issues PV
+constexpr int kIdxWarp = 10;
+constexpr int kProdWarp0 = 11;
+constexpr int kProdWarps = 5;       // row gathers from L2/HBM scale with the warps issuing them
+constexpr int kThreads = 32 * (kSmxWarps + 3 + kProdWarps);   // + QK, PV and index warps
+constexpr int kQuads = kRows / 4;   // producer work unit: 4 rows (one warp instruction per 128-byte piece)
+constexpr int kQuadsPerProd = (kQuads + kProdWarps - 1) / kProdWarps;
+// registers per thread: the launch gives every thread 128 (512 threads, one CTA
+// per SM); the two softmax warpgroups then take 168 and the two others give back
+// down to 88, which adds up to the launch's 65536 exactly
+constexpr int kSmxRegs = 168;
+constexpr int kOtherRegs = 88;
+static_assert(kThreads == 512 && 256 * kSmxRegs + 256 * kOtherRegs == 65536, "register split must add up");
+static_assert(kProdWarps >= 4, "scale words are fetched by four producer warps");
 constexpr int kRing = 4;            // tiles of translated rows kept ahead of the producers
 constexpr int kScStage = kRows * 16;   // scale words of one tile (528-byte rows)
 constexpr int kSmemLimit = 232448;
@@ -99,12 +109,12 @@ struct Misc {
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t q_full[2];         // a segment's query operand is built (by the softmax warps)
-  uint64_t p_full[2];
+  uint64_t p_full[2];         // P buffer b written (and O rescaled) by every softmax thread
   uint64_t pv_done[2];        // PV of the tiles that used P buffer b has completed
-  uint64_t mma_final;
+  uint64_t mma_final[2];      // drain of the QK^T and the PV issuer
   uint32_t tmem_base;
   int abort;
-  uint32_t vmask[3][4];       // valid-entry bits of each stage's tile: word k bit l = row 4l + k
+  uint8_t vflag[3][kRows];    // valid-entry flag of each row of each stage's tile
   __align__(16) int32_t ring[kRing][kRows];   // physical row of each entry (-1: masked)
   float red[2][2][4][16];     // [tile parity][head half][lane quarter][head] tile maxima
   float red_sc[2][4][4];      // [tile parity][lane quarter][group] maxima of the group scales
@@ -476,13 +486,14 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
   }
 }
 
-// Producers: copy the rows of each tile into its stage.  Warp pw owns tile
-// rows [64 pw, 64 pw + 64); one warp instruction moves 128-byte piece kb of
-// four rows (lane: row 4g + lane / 8, 16-byte chunk lane % 8).
+// Producers: copy the rows of each tile into its stage.  Producer warp pw
+// owns the row quads q = pw, pw + kProdWarps, ...; one warp instruction moves
+// 128-byte piece kb of the four rows of a quad (lane: row 4q + lane / 8,
+// 16-byte chunk lane % 8).  Scale words of 528-byte rows: warps 0-3, one row
+// per lane.
 template <int HG, bool kScaled, bool kQ8, bool kRope>
 __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it) {
   using C = Cfg<HG, kScaled, kQ8, kRope>;
-  constexpr int kRowsPerWarp = kRows / kProdWarps;   // 64
   constexpr int R = kRope ? kRopeRow : kScaled ? kScaledRow : kRawRow;
   const int ptid = threadIdx.x - kProdWarp0 * 32;
   const int pw = ptid >> 5, lane = ptid & 31;
@@ -493,32 +504,31 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
     const int stage = it % C::NST, slot = it % kRing;
     if (it >= C::NST && !warp_wait(smem_u32(&ms.kv_empty[stage]), ((it / C::NST) - 1) & 1, abort, a.wait_ns)) break;
     if (!warp_wait(smem_u32(&ms.idx_full[slot]), (it / kRing) & 1, abort, a.wait_ns)) break;
-    int32_t rows[kRowsPerWarp / 4];
+    int32_t rows[kQuadsPerProd];
 #pragma unroll
-    for (int g = 0; g < kRowsPerWarp / 4; ++g) rows[g] = ms.ring[slot][kRowsPerWarp * pw + 4 * g + rq];
-    int32_t sc_rows[kRowsPerWarp / 32];
-    if (kScaled) {
-#pragma unroll
-      for (int k = 0; k < kRowsPerWarp / 32; ++k) sc_rows[k] = ms.ring[slot][kRowsPerWarp * pw + 32 * k + lane];
+    for (int i = 0; i < kQuadsPerProd; ++i) {
+      const int q = pw + i * kProdWarps;
+      rows[i] = q < kQuads ? ms.ring[slot][4 * q + rq] : -1;
     }
+    const int32_t sc_row = (kScaled && pw < 4) ? ms.ring[slot][32 * pw + lane] : -1;
     mbar_arrive(smem_u32(&ms.idx_free[slot]));
-    // valid bits of the stage (its previous tile's softmax is done: PV of
-    // that tile released the stage): lane rq holds rows 4g + rq of this
-    // warp's half, i.e. bits 16 pw + g of word rq
-    {
-      uint32_t bits = 0;
+    // valid flags of the stage (its previous tile's softmax is done: PV of
+    // that tile released the stage)
 #pragma unroll
-      for (int g = 0; g < kRowsPerWarp / 4; ++g) bits |= (rows[g] >= 0 ? 1u : 0u) << g;
-      if (ch == 0) reinterpret_cast<uint16_t*>(&ms.vmask[stage][rq])[pw] = (uint16_t)bits;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ms.meta_full[stage]));
+    for (int i = 0; i < kQuadsPerProd; ++i) {
+      const int q = pw + i * kProdWarps;
+      if (q < kQuads && ch == 0) ms.vflag[stage][4 * q + rq] = rows[i] >= 0 ? 1 : 0;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ms.meta_full[stage]));
     const uint32_t base = kv0 + stage * kStage;
     const uint32_t rope_base = smem_u32(sm + C::ROPE_OFF) + stage * C::ROPE_STAGE;
 #pragma unroll
-    for (int g = 0; g < kRowsPerWarp / 4; ++g) {
-      const int r = kRowsPerWarp * pw + 4 * g + rq;
-      const int32_t row = rows[g];
+    for (int i = 0; i < kQuadsPerProd; ++i) {
+      const int q = pw + i * kProdWarps;
+      if (q >= kQuads) break;
+      const int r = 4 * q + rq;
+      const int32_t row = rows[i];
       const uint8_t* src = a.pool + (int64_t)(row >= 0 ? row : 0) * R + ch * 16;
       const uint32_t n = row >= 0 ? 16u : 0u;
       const uint32_t dst = base + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
@@ -528,128 +538,128 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
         cp_async_16_zfill(rope_base + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4),
                           src + kScaledRow, n);
     }
-    if (kScaled) {
-#pragma unroll
-      for (int k = 0; k < kRowsPerWarp / 32; ++k) {
-        const int r = kRowsPerWarp * pw + 32 * k + lane;
-        cp_async_16_zfill(smem_u32(sm + C::SC_OFF + stage * kScStage + r * 16),
-                          a.pool + (int64_t)(sc_rows[k] >= 0 ? sc_rows[k] : 0) * R + kD,
-                          sc_rows[k] >= 0 ? 16u : 0u);
-      }
+    if (kScaled && pw < 4) {
+      const int r = 32 * pw + lane;
+      cp_async_16_zfill(smem_u32(sm + C::SC_OFF + stage * kScStage + r * 16),
+                        a.pool + (int64_t)(sc_row >= 0 ? sc_row : 0) * R + kD, sc_row >= 0 ? 16u : 0u);
     }
     cp_async_arrive_noinc(smem_u32(&ms.kv_full[stage]));
   }
   cp_async_wait_all();
 }
 
+// A shared-memory descriptor moved `bytes` further (the start address field
+// holds address / 16 and never overflows inside the 227 KB window).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
+
+// PV of one tile: O^T += V^T P^T over the four 128-dim blocks of the tile,
+// K = 32 rows per MMA.  Descriptors are the stage's and the P buffer's base
+// descriptors plus compile-time offsets, so each MMA costs a few instructions
+// to issue.
+template <class C, bool kFirst>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint64_t ad0, uint64_t bd0, uint32_t idesc) {
+#pragma unroll
+  for (int db = 0; db < 4; ++db) {
+#pragma unroll
+    for (int js = 0; js < 4; ++js) {
+      // V^T: rows 32 js .. of dims block db (MN-major, 128-byte swizzle);
+      // P: rows 32 js .. = four groups of 8 rows (MN-major, no swizzle)
+      const uint64_t ad = desc_add(ad0, db * 16384 + js * 4096);
+      const uint64_t bd = desc_add(bd0, (C::G > 1 ? db * (C::NP * 128) : 0) + js * 4 * (C::NP * 8));
+      mma_e4m3(o_tmem + db * C::NP, ad, bd, idesc, (!kFirst || js > 0) ? 1u : 0u);
+    }
+  }
+}
+
+// Waits (bounded) for every tcgen05 operation this thread issued, so that the
+// tensor memory can be released.
+__device__ __forceinline__ void drain_mma(uint32_t bar) {
+  mma_commit(bar);
+  volatile int no_abort = 0;
+  mbar_wait(bar, 0, &no_abort, 2000000000ull);
+}
+
+// QK^T issuer (one thread): per tile chunk, once its stage, query operand and
+// score buffer are in place, S^T = K_tile Q^T into the score buffer.
 template <int HG, bool kScaled, bool kQ8, bool kRope>
-__device__ void mma_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it) {
+__device__ void qk_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it) {
   using C = Cfg<HG, kScaled, kQ8, kRope>;
   if ((threadIdx.x & 31) != 0) return;
   volatile int* abort = &ms.abort;
   const uint32_t kv0 = smem_u32(sm + C::KV_OFF);
   const uint32_t q0 = smem_u32(sm + C::Q_OFF);
-  const uint32_t p0 = smem_u32(sm + C::P_OFF);
   constexpr uint32_t kIdQK = idesc_e4m3(C::NQ, false);
-  constexpr uint32_t kIdPV = idesc_e4m3(C::NP, true, true);
   constexpr uint32_t kIdRope = idesc_bf16(C::NR > 0 ? C::NR : 16);
   const uint32_t rope0 = smem_u32(sm + C::ROPE_OFF);
   const uint32_t qr0 = smem_u32(sm + C::QR_OFF);
-  // Issue whichever is ready: PV of the oldest tile whose P is written, or
-  // the next QK^T chunk whose tile, query and score buffer are in place.
-  int qk_it = 0, qk_qc = 0, pv_j = 0, seg = -1;
-  bool q_ready = false, kv_ready = false;
-  TileCursor qk_cur(a, b0), pv_cur(a, b0);
-  uint64_t idle_since = globaltimer_ns();
-  while (pv_j < n_it) {
-    bool progressed = false;
-    if (pv_j < qk_it) {                                   // QK^T of tile pv_j fully issued
-      const int pb = pv_j % C::NPB;
-      if (mbar_test(smem_u32(&ms.p_full[pb]), (pv_j / C::NPB) & 1)) {
-        const bool pv_first = pv_cur.first(pv_j);
-        tc_fence_after();
-        const uint32_t a_base = kv0 + (pv_j % C::NST) * kStage;
-        const uint32_t b_base = p0 + pb * C::P_BYTES;
-#pragma unroll
-        for (int db = 0; db < 4; ++db) {
-#pragma unroll
-          for (int js = 0; js < 4; ++js) {
-            const uint64_t ad = sdesc_sw128(a_base + db * 16384 + js * 4096, 1024, 1024);
-            // rows 32 js .. 32 js + 31 of P: four groups of 8 rows
-            const uint64_t bd = sdesc_mn_none(b_base + (kScaled ? db * (C::NP * 128) : 0) + js * 4 * (C::NP * 8),
-                                              C::NP * 8, 128);
-            mma_e4m3(tmem + C::O_COL0 + db * C::NP, ad, bd, kIdPV, (!pv_first || js > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(smem_u32(&ms.kv_empty[pv_j % C::NST]));
-        mma_commit(smem_u32(&ms.pv_done[pb]));
-        ++pv_j;
-        pv_cur.advance(a);
-        progressed = true;
-      }
+  int seg = -1;
+  bool ok = true;
+  TileCursor cur(a, b0);
+  for (int it = 0; it < n_it && ok; ++it, cur.advance(a)) {
+    const int stage = it % C::NST;
+    if (cur.first(it)) {
+      ++seg;
+      ok = mbar_wait(smem_u32(&ms.q_full[seg % C::NQB]), (seg / C::NQB) & 1, abort, a.wait_ns);
     }
-    if (!progressed && qk_it < n_it) {
-      const bool qk_first = qk_cur.first(qk_it);
-      const int stage = qk_it % C::NST;
-      if (qk_qc == 0 && qk_first && !q_ready) {
-        if (mbar_test(smem_u32(&ms.q_full[(seg + 1) % C::NQB]), ((seg + 1) / C::NQB) & 1)) {
-          q_ready = true;
-          ++seg;
-        }
-      }
-      if (qk_qc == 0 && !kv_ready) kv_ready = mbar_test(smem_u32(&ms.kv_full[stage]), (qk_it / C::NST) & 1);
-      const int u = qk_it * C::NQC + qk_qc, sb = u % C::NS;
-      const bool q_ok = !(qk_qc == 0 && qk_first) || q_ready;
-      if (q_ok && kv_ready && (u < C::NS || mbar_test(smem_u32(&ms.s_free[sb]), ((u / C::NS) - 1) & 1))) {
-        fence_proxy_async_smem();   // rows landed through cp.async (generic proxy)
-        tc_fence_after();
-        const uint32_t a_base = kv0 + stage * kStage;
-        const uint32_t b_base = q0 + (seg % C::NQB) * C::Q_BYTES;
-        const uint32_t d_base = tmem + sb * C::S_COLS;
-        constexpr int kSteps = kScaled ? 4 * C::GC : 16;   // K = 32 per step
+    ok = ok && mbar_wait(smem_u32(&ms.kv_full[stage]), (it / C::NST) & 1, abort, a.wait_ns);
+    fence_proxy_async_smem();   // rows landed through cp.async (generic proxy)
+#pragma unroll 1
+    for (int qc = 0; qc < C::NQC && ok; ++qc) {
+      const int u = it * C::NQC + qc, sb = u % C::NS;
+      if (u >= C::NS) ok = mbar_wait(smem_u32(&ms.s_free[sb]), ((u / C::NS) - 1) & 1, abort, a.wait_ns);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t ad0 = sdesc_sw128(kv0 + stage * kStage + qc * (C::GC * 16384), 16, 1024);
+      const uint64_t bd0 = sdesc_sw128(q0 + (seg % C::NQB) * C::Q_BYTES + qc * (C::GC * C::NQ * 128), 16, 1024);
+      const uint32_t d_base = tmem + sb * C::S_COLS;
+      constexpr int kSteps = kScaled ? 4 * C::GC : 16;   // K = 32 per step
 #pragma unroll
-        for (int st = 0; st < kSteps; ++st) {
-          const int ks = qk_qc * kSteps + st;               // K step over the 512 dims
-          const int kb = ks >> 2, kk = ks & 3;
-          const uint64_t ad = sdesc_sw128(a_base + kb * 16384 + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b_base + kb * (C::NQ * 128) + kk * 32, 16, 1024);
-          const uint32_t d = d_base + (kScaled ? (kb - qk_qc * C::GC) * C::NQ : 0);
-          const uint32_t acc = kScaled ? (kk > 0 ? 1u : 0u) : (ks > 0 ? 1u : 0u);
-          mma_e4m3(d, ad, bd, kIdQK, acc);
-        }
-        if (kRope && qk_qc == 0) {
-          // S_rope = K_rope Q_rope^T: 64 BF16 dims, K = 16 per MMA
-          const uint32_t ra = rope0 + stage * C::ROPE_STAGE;
-          const uint32_t rb = qr0 + (seg % C::NQB) * C::QR_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(d_base + C::GC * C::NQ, sdesc_sw128(ra + kk * 32, 16, 1024), sdesc_sw128(rb + kk * 32, 16, 1024),
-                     kIdRope, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&ms.s_full[sb]));
-        if (++qk_qc == C::NQC) {
-          qk_qc = 0;
-          ++qk_it;
-          qk_cur.advance(a);
-          q_ready = false;
-          kv_ready = false;
-        }
-        progressed = true;
+      for (int st = 0; st < kSteps; ++st) {
+        const int kb = st >> 2, kk = st & 3;              // 128-dim block within the chunk, K step in it
+        const uint64_t ad = desc_add(ad0, kb * 16384 + kk * 32);
+        const uint64_t bd = desc_add(bd0, kb * (C::NQ * 128) + kk * 32);
+        // 528-byte rows: one accumulator per group (scaled by its rows' scales later)
+        mma_e4m3(d_base + (kScaled ? kb * C::NQ : 0), ad, bd, kIdQK, (kScaled ? kk > 0 : st > 0) ? 1u : 0u);
       }
-    }
-    if (progressed) {
-      idle_since = globaltimer_ns();
-    } else if (*abort) {
-      break;
-    } else if (globaltimer_ns() - idle_since > a.wait_ns) {
-      *abort = 1;
-      break;
+      if (kRope && qc == 0) {
+        // S_rope = K_rope Q_rope^T: 64 BF16 dims, K = 16 per MMA
+        const uint32_t ra = rope0 + stage * C::ROPE_STAGE;
+        const uint32_t rb = qr0 + (seg % C::NQB) * C::QR_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(d_base + C::GC * C::NQ, sdesc_sw128(ra + kk * 32, 16, 1024), sdesc_sw128(rb + kk * 32, 16, 1024),
+                   kIdRope, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&ms.s_full[sb]));
     }
   }
-  // every MMA of this CTA completes before the tensor memory is released
-  mma_commit(smem_u32(&ms.mma_final));
-  volatile int no_abort = 0;
-  mbar_wait(smem_u32(&ms.mma_final), 0, &no_abort, 2000000000ull);
+  drain_mma(smem_u32(&ms.mma_final[0]));
+}
+
+// PV issuer (one thread): per tile, once every softmax thread has written its
+// P rows; its commits release the P buffer and the stage.
+template <int HG, bool kScaled, bool kQ8, bool kRope>
+__device__ void pv_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem, int64_t b0, int n_it) {
+  using C = Cfg<HG, kScaled, kQ8, kRope>;
+  if ((threadIdx.x & 31) != 0) return;
+  volatile int* abort = &ms.abort;
+  const uint32_t kv0 = smem_u32(sm + C::KV_OFF);
+  const uint32_t p0 = smem_u32(sm + C::P_OFF);
+  constexpr uint32_t kIdPV = idesc_e4m3(C::NP, true, true);
+  TileCursor cur(a, b0);
+  for (int it = 0; it < n_it; ++it, cur.advance(a)) {
+    const int pb = it % C::NPB, stage = it % C::NST;
+    if (!mbar_wait(smem_u32(&ms.p_full[pb]), (it / C::NPB) & 1, abort, a.wait_ns)) break;
+    fence_proxy_async_smem();   // P and the stage were written through the generic proxy
+    tc_fence_after();
+    const uint64_t ad0 = sdesc_sw128(kv0 + stage * kStage, 1024, 1024);
+    const uint64_t bd0 = sdesc_mn_none(p0 + pb * C::P_BYTES, C::NP * 8, 128);
+    if (cur.first(it)) issue_pv<C, true>(tmem + C::O_COL0, ad0, bd0, kIdPV);
+    else issue_pv<C, false>(tmem + C::O_COL0, ad0, bd0, kIdPV);
+    mma_commit(smem_u32(&ms.kv_empty[stage]));
+    mma_commit(smem_u32(&ms.pv_done[pb]));
+  }
+  drain_mma(smem_u32(&ms.mma_final[1]));
 }
 
 // Loads columns [c, c + HPT) of a 32-lane TMEM slice, HPT in {4, 8, 16}.
@@ -724,7 +734,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     }
     const int qb = seg % C::NQB;
     ok &= mbar_wait(smem_u32(&ms.meta_full[stage]), (it / C::NST) & 1, abort, a.wait_ns);
-    const bool valid = (ms.vmask[stage][row & 3] >> (row >> 2)) & 1u;
+    const bool valid = ms.vflag[stage][row] != 0;
     float sc4[4] = {1.f, 1.f, 1.f, 1.f};
     if (kScaled) {
       ok &= mbar_wait(smem_u32(&ms.kv_full[stage]), (it / C::NST) & 1, abort, a.wait_ns);
@@ -977,9 +987,16 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   (void)ok;
 }
 
-// 12 warps: three share a sub-partition's 16K registers, so at most 168 each.
+// Register re-split after the launch (see kSmxRegs): executed by whole warpgroups.
+__device__ __forceinline__ void regs_inc_smx() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSmxRegs));
+}
+__device__ __forceinline__ void regs_dec_other() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+}
+
 template <int HG, bool kScaled, bool kQ8, bool kRope>
-__global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   using C = Cfg<HG, kScaled, kQ8, kRope>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1006,11 +1023,12 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
       mbar_init(smem_u32(&ms.p_full[s]), kSmxThreads);
       mbar_init(smem_u32(&ms.pv_done[s]), 1);
     }
-    mbar_init(smem_u32(&ms.mma_final), 1);
+    mbar_init(smem_u32(&ms.mma_final[0]), 1);
+    mbar_init(smem_u32(&ms.mma_final[1]), 1);
     ms.abort = 0;
     mbar_init_fence();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tmem_alloc(smem_u32(&ms.tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -1031,10 +1049,16 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
   // of this grid exit and wait for the whole grid before reading partials
   grid_launch_dependents();
 
+  // 16 warps: softmax warpgroups 0-1 grow to kSmxRegs registers a thread, the
+  // MMA / index / producer warpgroups 2-3 shrink to kOtherRegs
+  if (warp < kSmxWarps) regs_inc_smx();
+  else regs_dec_other();
   if (warp < kSmxWarps)
     softmax_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it, cta);
-  else if (warp == kMmaWarp)
-    mma_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it);
+  else if (warp == kQkWarp)
+    qk_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it);
+  else if (warp == kPvWarp)
+    pv_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it);
   else if (warp == kIdxWarp)
     index_role<HG, kScaled, kQ8, kRope>(a, sm, ms, b0, n_it);
   else
@@ -1042,7 +1066,7 @@ __global__ void __maxnreg__(168) sparse_attn_tc_kernel(const __grid_constant__ A
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
