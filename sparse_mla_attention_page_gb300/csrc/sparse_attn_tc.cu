@@ -76,6 +76,8 @@ using namespace tc;
 constexpr int kRows = 128;          // top-k entries per tile = MMA M
 constexpr int kStage = 65536;       // one tile: 128 rows x 512 FP8 bytes
 constexpr float kTau = 8.0f;        // lazy max threshold (log2 units)
+constexpr float kNoMax = -1.0e30f;  // running max of a head with no valid entry yet (finite, so
+                                    // 2^(s - m) needs no guard: masked s = -inf gives 0)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSmxWarps = 8;        // softmax warps: warp w -> lane quarter w % 4, head half w / 4
@@ -723,7 +725,8 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
   volatile int* abort = &ms.abort;
   float m_run[HPT], l_part[HPT];
-  float m_lane = -INFINITY;        // running max of head hbase + (lane % HPT), log2 units
+  float m_thr[HPT];                // m_run + kTau: a score above it makes the running max grow
+  float m_lane = kNoMax;           // running max of head hbase + (lane % HPT), log2 units
   int e_grp[4] = {-1000, -1000, -1000, -1000};   // running scale exponents (528-byte rows)
   int seg = -1;
   bool ok = true;                  // false once a wait gave up: keep going through every barrier
@@ -741,10 +744,11 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       ++seg;
       const int qb = seg % C::NQB;
       ok &= mbar_wait(smem_u32(&ms.q_full[qb]), (seg / C::NQB) & 1, abort, a.wait_ns);
-      m_lane = -INFINITY;
+      m_lane = kNoMax;
 #pragma unroll
       for (int h = 0; h < HPT; ++h) {
-        m_run[h] = -INFINITY;
+        m_run[h] = kNoMax;
+        m_thr[h] = kNoMax + kTau;
         l_part[h] = 0.f;
       }
 #pragma unroll
@@ -775,10 +779,20 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
         tmem_ld_cols<HPT>(cbase + hbase, hi);
         if (!kQ8) tmem_ld_cols<HPT>(cbase + HG + hbase, lo);
         tmem_wait_ld();
+        float qs_hi[HPT], qs_lo[HPT];   // score column multipliers (16-byte aligned runs)
+#pragma unroll
+        for (int k = 0; k < HPT; k += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(&ms.qsig[qb][hbase + k]);
+          qs_hi[k] = m4.x; qs_hi[k + 1] = m4.y; qs_hi[k + 2] = m4.z; qs_hi[k + 3] = m4.w;
+          if (!kQ8) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&ms.qsig[qb][HG + hbase + k]);
+            qs_lo[k] = l4.x; qs_lo[k + 1] = l4.y; qs_lo[k + 2] = l4.z; qs_lo[k + 3] = l4.w;
+          }
+        }
 #pragma unroll
         for (int k = 0; k < HPT; ++k) {
-          float v = __uint_as_float(hi[k]) * ms.qsig[qb][hbase + k];
-          if (!kQ8) v = fmaf(__uint_as_float(lo[k]), ms.qsig[qb][HG + hbase + k], v);
+          float v = __uint_as_float(hi[k]) * qs_hi[k];
+          if (!kQ8) v = fmaf(__uint_as_float(lo[k]), qs_lo[k], v);
           s2[k] = kScaled ? fmaf(sc4[g], v, s2[k]) : v;
         }
       }
@@ -811,7 +825,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     // exchange it saves (measured), so their tiles always form the maxima.
     bool grow = false;
 #pragma unroll
-    for (int h = 0; h < HPT; ++h) grow |= s2[h] > m_run[h] + kTau;
+    for (int h = 0; h < HPT; ++h) grow |= s2[h] > m_thr[h];
     float tmp[HPT];
     unsigned rmask = 0;
     float alpha_lane = 1.f;
@@ -844,6 +858,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
         for (int h = 0; h < HPT; ++h) {
           m_run[h] = __shfl_sync(0xffffffffu, m_lane, h);
+          m_thr[h] = m_run[h] + kTau;
           l_part[h] *= __shfl_sync(0xffffffffu, alpha_lane, h);
         }
       }
@@ -893,7 +908,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     // p = 2^(s - m) (0 while the head has seen no valid entry), denominators, P operand
 #pragma unroll
     for (int h = 0; h < HPT; ++h) {
-      s2[h] = m_run[h] == -INFINITY ? 0.f : ex2_approx(s2[h] - m_run[h]);
+      s2[h] = ex2_approx(s2[h] - m_run[h]);
       l_part[h] += s2[h];
     }
     // three E4M3 terms of a pair of P values: v ~ hi + mid / 16 + lo / 256
