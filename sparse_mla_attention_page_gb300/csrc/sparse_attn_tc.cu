@@ -91,11 +91,9 @@ constexpr int kThreads = 32 * (kSmxWarps + 3 + kProdWarps);   // + QK, PV and in
 constexpr int kQuads = kRows / 4;   // producer work unit: 4 rows (one warp instruction per 128-byte piece)
 constexpr int kQuadsPerProd = (kQuads + kProdWarps - 1) / kProdWarps;
 // registers per thread: the launch gives every thread 128 (512 threads, one CTA
-// per SM); the two softmax warpgroups then take 168 and the two others give back
-// down to 88, which adds up to the launch's 65536 exactly
-constexpr int kSmxRegs = 168;
-constexpr int kOtherRegs = 88;
-static_assert(kThreads == 512 && 256 * kSmxRegs + 256 * kOtherRegs == 65536, "register split must add up");
+// per SM); the two softmax warpgroups then take Cfg::SMX_REGS and the two others
+// give back down to 256 - SMX_REGS, which adds up to the launch's 65536 exactly
+static_assert(kThreads == 512, "register split assumes 512 threads");
 static_assert(kProdWarps >= 4, "scale words are fetched by four producer warps");
 constexpr int kRing = 4;            // tiles of translated rows kept ahead of the producers
 constexpr int kScStage = kRows * 16;   // scale words of one tile (528-byte rows)
@@ -176,6 +174,10 @@ struct Cfg {
   static constexpr int SC_OFF = ROPE_OFF + NST * ROPE_STAGE;
   static constexpr int MISC_OFF = SC_OFF + (kScaled ? NST * kScStage : 0);
   static constexpr int SMEM = MISC_OFF + kMiscBytes + 1024;
+  // softmax / other warpgroups' registers a thread (measured spill-free or least
+  // spilling split per instantiation; the two add up to 256)
+  static constexpr int SMX_REGS = HG <= 16 ? 152 : (!kScaled && !kQ8) ? 176 : 168;
+  static constexpr int OTHER_REGS = 256 - SMX_REGS;
   static_assert(HPT >= 4 && HPT <= 16, "heads per softmax thread");
   static_assert(USED <= 512, "tensor memory budget");
   static_assert(SMEM <= kSmemLimit, "shared memory budget");
@@ -1015,12 +1017,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   (void)ok;
 }
 
-// Register re-split after the launch (see kSmxRegs): executed by whole warpgroups.
-__device__ __forceinline__ void regs_inc_smx() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSmxRegs));
+// Register re-split after the launch (Cfg::SMX_REGS): executed by whole warpgroups.
+template <int kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
-__device__ __forceinline__ void regs_dec_other() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+template <int kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 template <int HG, bool kScaled, bool kQ8, bool kRope>
@@ -1077,10 +1081,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const __gri
   // of this grid exit and wait for the whole grid before reading partials
   grid_launch_dependents();
 
-  // 16 warps: softmax warpgroups 0-1 grow to kSmxRegs registers a thread, the
-  // MMA / index / producer warpgroups 2-3 shrink to kOtherRegs
-  if (warp < kSmxWarps) regs_inc_smx();
-  else regs_dec_other();
+  // 16 warps: softmax warpgroups 0-1 grow to SMX_REGS registers a thread, the
+  // MMA / index / producer warpgroups 2-3 shrink to OTHER_REGS
+  static_assert(C::SMX_REGS % 8 == 0 && C::SMX_REGS >= 128 && C::OTHER_REGS >= 24, "setmaxnreg values");
+  if (warp < kSmxWarps) regs_inc<C::SMX_REGS>();
+  else regs_dec<C::OTHER_REGS>();
   if (warp < kSmxWarps)
     softmax_role<HG, kScaled, kQ8, kRope>(a, sm, ms, tmem, b0, n_it, cta);
   else if (warp == kQkWarp)
