@@ -139,8 +139,9 @@ int sparse_attn(bool q8, const void* q, const float* q_scale, int T, int H, int 
   a.err = err;
   a.wait_ns = g_wait_ns.load();
   cudaGetLastError();
-  dsa::launch_sparse_attn(a, q8, static_cast<cudaStream_t>(stream));
-  return launch_status();
+  const bool launched = dsa::launch_sparse_attn(a, q8, static_cast<cudaStream_t>(stream));
+  const int st2 = launch_status();
+  return st2 != DSA_OK ? st2 : launched ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace

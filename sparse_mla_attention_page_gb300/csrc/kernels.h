@@ -56,7 +56,9 @@ struct AttnPlan {
 };
 AttnPlan plan_attn(int T, int H, int K, int sms, bool rope);
 
-void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
+// false when nothing was launched (a launch attribute could not be set, or the
+// kernel was not built with the register count its register re-split needs).
+bool launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream);
 
 // Gather / dequantise reader (see gather_dequant.cu).
 struct GatherArgs {

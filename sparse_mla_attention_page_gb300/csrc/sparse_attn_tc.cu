@@ -80,20 +80,22 @@ constexpr float kNoMax = -1.0e30f;  // running max of a head with no valid entry
                                     // 2^(s - m) needs no guard: masked s = -inf gives 0)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kSmxWarps = 8;        // softmax warps: warp w -> lane quarter w % 4, head half w / 4
+constexpr int kSmxWarps = 16;       // softmax warps: warp w -> lane quarter w % 4, head quarter w / 4
 constexpr int kSmxThreads = kSmxWarps * 32;
-constexpr int kQkWarp = 8;          // issues QK^T
-constexpr int kPvWarp = 9;          // issues PV
-constexpr int kIdxWarp = 10;
-constexpr int kProdWarp0 = 11;
+constexpr int kQkWarp = 16;         // issues QK^T
+constexpr int kPvWarp = 17;         // issues PV
+constexpr int kIdxWarp = 18;
+constexpr int kProdWarp0 = 19;
 constexpr int kProdWarps = 5;       // row gathers from L2/HBM scale with the warps issuing them
 constexpr int kThreads = 32 * (kSmxWarps + 3 + kProdWarps);   // + QK, PV and index warps
 constexpr int kQuads = kRows / 4;   // producer work unit: 4 rows (one warp instruction per 128-byte piece)
 constexpr int kQuadsPerProd = (kQuads + kProdWarps - 1) / kProdWarps;
-// registers per thread: the launch gives every thread 128 (512 threads, one CTA
-// per SM); the two softmax warpgroups then take Cfg::SMX_REGS and the two others
-// give back down to 256 - SMX_REGS, which adds up to the launch's 65536 exactly
-static_assert(kThreads == 512, "register split assumes 512 threads");
+// registers per thread: the launch gives every thread 80 (768 threads, one CTA
+// per SM, 24 warps of 10 x 256 registers); the four softmax warpgroups then take
+// Cfg::SMX_REGS and the two others give back down to Cfg::OTHER_REGS, the two
+// adding up to the launch's 61440 exactly
+constexpr int kLaunchRegs = 80;
+static_assert(kThreads == 768 && kSmxThreads == 512, "register split assumes 768 threads");
 static_assert(kProdWarps >= 4, "scale words are fetched by four producer warps");
 constexpr int kRing = 4;            // tiles of translated rows kept ahead of the producers
 constexpr int kScStage = kRows * 16;   // scale words of one tile (528-byte rows)
@@ -116,9 +118,9 @@ struct Misc {
   int abort;
   uint8_t vflag[3][kRows];    // valid-entry flag of each row of each stage's tile
   __align__(16) int32_t ring[kRing][kRows];   // physical row of each entry (-1: masked)
-  float red[2][2][4][16];     // [tile parity][head half][lane quarter][head] tile maxima
+  float red[2][4][4][8];      // [tile parity][head quarter][lane quarter][head] tile maxima
   float red_sc[2][4][4];      // [tile parity][lane quarter][group] maxima of the group scales
-  float red2[2][4][16];       // [head half][lane quarter][head] denominators (epilogue)
+  float red2[4][4][8];        // [head quarter][lane quarter][head] denominators (epilogue)
   __align__(16) float qsig[2][64];   // log2-domain multiplier of each score column, per query buffer
   float linv[32], lse2[32];
 };
@@ -127,7 +129,7 @@ static_assert(offsetof(Misc, ring) % 16 == 0 && offsetof(Misc, qsig) % 16 == 0, 
 
 template <int HG, bool kScaled, bool kQ8, bool kRope>
 struct Cfg {
-  static constexpr int HPT = HG / 2;                           // heads per softmax thread
+  static constexpr int HPT = HG / 4;                           // heads per softmax thread
   static constexpr int G = kScaled ? 4 : 1;                    // score accumulators per tile
   static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : 2 * HG;  // QK^T N (query operand rows)
   static constexpr int NP = (3 * HG + 15) / 16 * 16;          // PV N: P hi, mid, lo rows (+ zero pad)
@@ -176,9 +178,9 @@ struct Cfg {
   static constexpr int SMEM = MISC_OFF + kMiscBytes + 1024;
   // softmax / other warpgroups' registers a thread (measured spill-free or least
   // spilling split per instantiation; the two add up to 256)
-  static constexpr int SMX_REGS = HG <= 16 ? 152 : (!kScaled && !kQ8) ? 176 : 168;
-  static constexpr int OTHER_REGS = 256 - SMX_REGS;
-  static_assert(HPT >= 4 && HPT <= 16, "heads per softmax thread");
+  static constexpr int SMX_REGS = HG <= 16 ? 88 : 96;
+  static constexpr int OTHER_REGS = (kLaunchRegs * kThreads - SMX_REGS * kSmxThreads) / (kThreads - kSmxThreads);
+  static_assert(HPT >= 2 && HPT <= 8, "heads per softmax thread");
   static_assert(USED <= 512, "tensor memory budget");
   static_assert(SMEM <= kSmemLimit, "shared memory budget");
   static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && (NP * 128) % 1024 == 0, "operand alignment");
@@ -241,6 +243,9 @@ __device__ __forceinline__ void split3_f16(float v0, float v1, uint32_t& hi2, ui
   lo2 = h;
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((uint16_t)v) : "memory");
+}
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -324,7 +329,8 @@ struct TileCursor {
 // stay zero).  Thread -> head tid / TPH, dims [DPT (tid % TPH), + DPT).
 template <int HG, bool kQ8, bool kRope>
 struct QueryBuild {
-  static constexpr int TPH = kSmxThreads / HG;           // threads per head
+  static constexpr int kThr = kSmxThreads < 32 * HG ? kSmxThreads : 32 * HG;   // threads that build
+  static constexpr int TPH = kThr / HG;                   // threads per head (one warp at most)
   static constexpr int DPT = kD / TPH;                    // dims per thread
   static constexpr int NV = kQ8 ? DPT / 16 : DPT / 8;     // 16-byte loads per thread
   static constexpr int NR = kRope ? (HG < 16 ? 16 : HG) : 0;   // RoPE operand rows (zero past HG)
@@ -334,12 +340,14 @@ struct QueryBuild {
 
   __device__ __forceinline__ void load(const AttnArgs& a, int t, int h0) {
     const int head = threadIdx.x / TPH, part = threadIdx.x % TPH;
-    const int64_t th = (int64_t)t * a.H + h0 + head;
-    const uint4* src = kQ8 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + th * kD + part * DPT)
-                           : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * a.q_row + part * DPT);
+    if (threadIdx.x < kThr) {        // whole warps
+      const int64_t th = (int64_t)t * a.H + h0 + head;
+      const uint4* src = kQ8 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + th * kD + part * DPT)
+                             : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + th * a.q_row + part * DPT);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
-    qs = kQ8 ? __ldg(a.q_scale + th) : 0.f;
+      for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
+      qs = kQ8 ? __ldg(a.q_scale + th) : 0.f;
+    }
     if constexpr (kRope) {
       const int rh = threadIdx.x >> 3, rc = threadIdx.x & 7;   // head, 16-byte chunk of its 64 dims
       rv = make_uint4(0, 0, 0, 0);
@@ -361,6 +369,7 @@ struct QueryBuild {
       if (rh < NR)
         *reinterpret_cast<uint4*>(rbuf + (rh >> 3) * 1024 + (rh & 7) * 128 + ((rc ^ (rh & 7)) << 4)) = rv;
     }
+    if (threadIdx.x >= kThr) return;   // whole warps
     if constexpr (kQ8) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(head, part * DPT + 16 * i)) = v[i];
@@ -687,7 +696,9 @@ __device__ void pv_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem,
 // Loads columns [c, c + HPT) of a 32-lane TMEM slice, HPT in {4, 8, 16}.
 template <int HPT>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[HPT]) {
-  if constexpr (HPT == 4) {
+  if constexpr (HPT == 2) {
+    tmem_ld2(taddr, v);
+  } else if constexpr (HPT == 4) {
     tmem_ld4(taddr, v);
   } else {
 #pragma unroll
@@ -702,7 +713,9 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[HPT])
 
 template <int HPT>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[HPT]) {
-  if constexpr (HPT == 4) {
+  if constexpr (HPT == 2) {
+    tmem_st2(taddr, v);
+  } else if constexpr (HPT == 4) {
     tmem_st4(taddr, v);
   } else {
 #pragma unroll
@@ -721,9 +734,9 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   using C = Cfg<HG, kScaled, kQ8, kRope>;
   constexpr int HPT = C::HPT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quarter = warp & 3, hh = warp >> 2;
+  const int quarter = warp & 3, hq = warp >> 2;         // TMEM lane quarter, head quarter
   const int row = 32 * quarter + lane;                    // tile row = TMEM lane
-  const int hbase = hh * HPT;                             // first head of this thread
+  const int hbase = hq * HPT;                             // first head of this thread
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
   volatile int* abort = &ms.abort;
   float m_run[HPT], l_part[HPT];
@@ -838,8 +851,8 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
       for (int h = 0; h < HPT; ++h) tmp[h] = s2[h];
       const float wmax = transpose_reduce<HPT, true>(tmp, lane);
-      if (lane < HPT) ms.red[it & 1][hh][quarter][lane] = wmax;
-      if (kScaled && hh == 0) {
+      if (lane < HPT) ms.red[it & 1][hq][quarter][lane] = wmax;
+      if (kScaled && hq == 0) {
         float sct[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) sct[g] = valid ? fabsf(sc4[g]) : 0.f;
@@ -848,8 +861,8 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       }
       named_bar_sync(1, kSmxThreads);
       const int hl = lane % HPT;
-      const float tile_max = fmaxf(fmaxf(ms.red[it & 1][hh][0][hl], ms.red[it & 1][hh][1][hl]),
-                                   fmaxf(ms.red[it & 1][hh][2][hl], ms.red[it & 1][hh][3][hl]));
+      const float tile_max = fmaxf(fmaxf(ms.red[it & 1][hq][0][hl], ms.red[it & 1][hq][1][hl]),
+                                   fmaxf(ms.red[it & 1][hq][2][hl], ms.red[it & 1][hq][3][hl]));
       const bool need = tile_max > m_lane + kTau;
       rmask = __ballot_sync(0xffffffffu, need);
       if (need) {
@@ -921,12 +934,12 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     // store: they are consecutive in the MN-major operand
     auto store_term = [&](uint32_t pg, int term, const uint32_t (&t2)[HPT / 2]) {
       const uint32_t addr = pg + p_off<C::NP>(term * HG + hbase, row);
-      if constexpr (HPT == 16)
-        st_shared_v4(addr, t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16), t2[4] | (t2[5] << 16), t2[6] | (t2[7] << 16));
-      else if constexpr (HPT == 8)
+      if constexpr (HPT == 8)
         st_shared_v2(addr, t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16));
-      else
+      else if constexpr (HPT == 4)
         st_shared_u32(addr, t2[0] | (t2[1] << 16));
+      else
+        st_shared_u16(addr, t2[0]);
     };
     if constexpr (kLateWait) {
       uint32_t hi2[HPT / 2], mid2[HPT / 2], lo2[HPT / 2];
@@ -966,10 +979,10 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
     for (int h = 0; h < HPT; ++h) tmp[h] = l_part[h];
     const float wsum = transpose_reduce<HPT, false>(tmp, lane);
-    if (lane < HPT) ms.red2[hh][quarter][lane] = wsum;
+    if (lane < HPT) ms.red2[hq][quarter][lane] = wsum;
     named_bar_sync(1, kSmxThreads);
     if (quarter == 0 && lane < HPT) {
-      const float l = (ms.red2[hh][0][lane] + ms.red2[hh][1][lane]) + (ms.red2[hh][2][lane] + ms.red2[hh][3][lane]);
+      const float l = (ms.red2[hq][0][lane] + ms.red2[hq][1][lane]) + (ms.red2[hq][2][lane] + ms.red2[hq][3][lane]);
       ms.linv[hbase + lane] = l > 0.f ? 1.f / l : 0.f;
       ms.lse2[hbase + lane] = l > 0.f ? m_lane + log2f(l) : -INFINITY;
     }
@@ -1083,7 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const __gri
 
   // 16 warps: softmax warpgroups 0-1 grow to SMX_REGS registers a thread, the
   // MMA / index / producer warpgroups 2-3 shrink to OTHER_REGS
-  static_assert(C::SMX_REGS % 8 == 0 && C::SMX_REGS >= 128 && C::OTHER_REGS >= 24, "setmaxnreg values");
+  static_assert(C::SMX_REGS % 8 == 0 && C::OTHER_REGS % 8 == 0 && C::SMX_REGS > kLaunchRegs &&
+                C::OTHER_REGS < kLaunchRegs && C::OTHER_REGS >= 24 &&
+                C::SMX_REGS * kSmxThreads + C::OTHER_REGS * (kThreads - kSmxThreads) == kLaunchRegs * kThreads,
+                "setmaxnreg values");
   if (warp < kSmxWarps) regs_inc<C::SMX_REGS>();
   else regs_dec<C::OTHER_REGS>();
   if (warp < kSmxWarps)
@@ -1107,7 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const __gri
 }
 
 template <int HG, bool kScaled, bool kQ8, bool kRope>
-void launch_tc(const AttnArgs& a, cudaStream_t stream) {
+bool launch_tc(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<HG, kScaled, kQ8, kRope>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -1116,7 +1132,14 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
   if (!(configured.load() & bit)) {
     if (cudaFuncSetAttribute(sparse_attn_tc_kernel<HG, kScaled, kQ8, kRope>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-      return;   // the launch below is skipped; the caller sees the attribute error
+      return false;   // the launch is skipped; the caller sees the attribute error
+    // the in-kernel register re-split adds up only if every thread starts with
+    // exactly kLaunchRegs registers; otherwise a warpgroup could wait forever
+    // for registers, so refuse to launch
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, sparse_attn_tc_kernel<HG, kScaled, kQ8, kRope>) != cudaSuccess ||
+        fa.numRegs != kLaunchRegs)
+      return false;
     configured.fetch_or(bit);
   }
   // programmatic dependent launch: the set-up (barriers, tensor memory,
@@ -1131,23 +1154,25 @@ void launch_tc(const AttnArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<HG, kScaled, kQ8, kRope>, a);
+  return cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<HG, kScaled, kQ8, kRope>, a) == cudaSuccess;
 }
 
 template <int HG>
-void launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
+bool launch_hg(const AttnArgs& a, bool q8, cudaStream_t stream) {
+  bool ok = false;
   if (a.rope) {
-    if constexpr (HG <= 16) launch_tc<HG, true, false, true>(a, stream);   // head_group caps HG at 16
+    if constexpr (HG <= 16) ok = launch_tc<HG, true, false, true>(a, stream);   // head_group caps HG at 16
   } else if (q8 && a.scaled) {
-    launch_tc<HG, true, true, false>(a, stream);
+    ok = launch_tc<HG, true, true, false>(a, stream);
   } else if (q8) {
-    launch_tc<HG, false, true, false>(a, stream);
+    ok = launch_tc<HG, false, true, false>(a, stream);
   } else if (a.scaled) {
-    launch_tc<HG, true, false, false>(a, stream);
+    ok = launch_tc<HG, true, false, false>(a, stream);
   } else {
-    launch_tc<HG, false, false, false>(a, stream);
+    ok = launch_tc<HG, false, false, false>(a, stream);
   }
-  if (a.ws_o != nullptr) launch_combine(a, stream);
+  if (ok && a.ws_o != nullptr) launch_combine(a, stream);
+  return ok;
 }
 
 }  // namespace
@@ -1157,10 +1182,10 @@ int head_group(int H, bool rope) {
   return H < cap ? H : cap;
 }
 
-void launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream) {
-  if (a.hg == 8) launch_hg<8>(a, q8, stream);
-  else if (a.hg == 16) launch_hg<16>(a, q8, stream);
-  else launch_hg<32>(a, q8, stream);
+bool launch_sparse_attn(const AttnArgs& a, bool q8, cudaStream_t stream) {
+  if (a.hg == 8) return launch_hg<8>(a, q8, stream);
+  if (a.hg == 16) return launch_hg<16>(a, q8, stream);
+  return launch_hg<32>(a, q8, stream);
 }
 
 }  // namespace dsa
