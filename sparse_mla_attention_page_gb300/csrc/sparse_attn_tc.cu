@@ -284,6 +284,15 @@ __device__ __forceinline__ float scale_pow2(float x, int e) {
   return __fmul_rn(__fmul_rn(x, __int_as_float((127 + e1) << 23)), __int_as_float((127 + e2) << 23));
 }
 
+// One arrival per warp on `bar`, after every lane's prior accesses (the
+// caller fences them for the proxy they feed first): mbarriers fed by whole
+// thread groups would otherwise take one serialised shared-memory atomic per
+// thread.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Warp-uniform bounded wait (all lanes agree on the outcome).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   const bool ok = mbar_wait(bar, parity, abort, limit_ns);
@@ -503,7 +512,7 @@ __device__ void index_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int64_t b0,
     const int slot = it % kRing;
     if (it >= kRing && !warp_wait(smem_u32(&ms.idx_free[slot]), ((it / kRing) - 1) & 1, abort, a.wait_ns)) break;
     *reinterpret_cast<int4*>(&ms.ring[slot][4 * lane]) = make_int4(rows[0], rows[1], rows[2], rows[3]);
-    mbar_arrive(smem_u32(&ms.idx_full[slot]));
+    warp_arrive(smem_u32(&ms.idx_full[slot]));
     // entries of tile it + 1 + kAhead; page-table reads of tile it + 1
     const int4 nxt = win[0];
     const int nxt_sq = wseq[0];
@@ -542,7 +551,7 @@ __device__ void producer_role(const AttnArgs& a, uint8_t* sm, Misc& ms, int n_it
       rows[i] = q < kQuads ? ms.ring[slot][4 * q + rq] : -1;
     }
     const int32_t sc_row = (kScaled && pw < 4) ? ms.ring[slot][32 * pw + lane] : -1;
-    mbar_arrive(smem_u32(&ms.idx_free[slot]));
+    warp_arrive(smem_u32(&ms.idx_free[slot]));
     // valid flags of the stage (its previous tile's softmax is done: PV of
     // that tile released the stage)
 #pragma unroll
@@ -750,7 +759,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   qnext.load(a, cur.t, cur.hgi * a.hg);
   qnext.template store<C::NQ>(a, sm + C::Q_OFF, ms.qsig[0], sm + C::QR_OFF);
   fence_proxy_async_smem();
-  mbar_arrive(smem_u32(&ms.q_full[0]));
+  warp_arrive(smem_u32(&ms.q_full[0]));
   for (int it = 0; it < n_it; ++it, cur.advance(a)) {
     const bool first = cur.first(it), last = cur.last(a, it, n_it);
     const int stage = it % C::NST, pb = it % C::NPB;
@@ -820,7 +829,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
         for (int k = 0; k < HPT; ++k) s2[k] = fmaf(__uint_as_float(rv[k]), rsig, s2[k]);
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&ms.s_free[sb]));
+      warp_arrive(smem_u32(&ms.s_free[sb]));
     }
     // the next segment's query: its loads fly while this tile's P is formed
     if (build_next) {
@@ -964,14 +973,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    mbar_arrive(smem_u32(&ms.p_full[pb]));
+    warp_arrive(smem_u32(&ms.p_full[pb]));
     // every thread passed this tile's barrier after its last read of the scores'
     // multipliers, and QK^T of this tile (the last reader of the operand) is done
     if (build_next) {
       const int nqb = (seg + 1) % C::NQB;
       qnext.template store<C::NQ>(a, sm + C::Q_OFF + nqb * C::Q_BYTES, ms.qsig[nqb], sm + C::QR_OFF + nqb * C::QR_BYTES);
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&ms.q_full[nqb]));
+      warp_arrive(smem_u32(&ms.q_full[nqb]));
     }
 
     if (!last) continue;
@@ -1058,14 +1067,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const __gri
       mbar_init(smem_u32(&ms.meta_full[s]), kProdWarps);
     }
     for (int s = 0; s < kRing; ++s) {
-      mbar_init(smem_u32(&ms.idx_full[s]), 32);
-      mbar_init(smem_u32(&ms.idx_free[s]), kProdWarps * 32);
+      mbar_init(smem_u32(&ms.idx_full[s]), 1);            // the index warp (one arrival a warp)
+      mbar_init(smem_u32(&ms.idx_free[s]), kProdWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ms.s_full[s]), 1);
-      mbar_init(smem_u32(&ms.s_free[s]), kSmxThreads);
-      mbar_init(smem_u32(&ms.q_full[s]), kSmxThreads);
-      mbar_init(smem_u32(&ms.p_full[s]), kSmxThreads);
+      mbar_init(smem_u32(&ms.s_free[s]), kSmxWarps);
+      mbar_init(smem_u32(&ms.q_full[s]), kSmxWarps);
+      mbar_init(smem_u32(&ms.p_full[s]), kSmxWarps);
       mbar_init(smem_u32(&ms.pv_done[s]), 1);
     }
     mbar_init(smem_u32(&ms.mma_final[0]), 1);
