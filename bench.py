@@ -524,64 +524,10 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     sampler.stop()
     total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
 
-    # end to end through the public API: the step's inputs from one pinned host
-    # buffer (one H2D copy), the results back in one D2H copy
-    def packed(parts):
-        """Byte offsets of 256-byte-aligned parts in one buffer, and its size."""
-        offs, n = [], 0
-        for a in parts:
-            offs.append(n)
-            n += (a.nbytes + 255) // 256 * 256
-        return offs, n
-
-    in_parts = [np.ascontiguousarray(w["q_bf16"]), np.ascontiguousarray(w["topk"]),
-                np.ascontiguousarray(case.x_new_h), np.ascontiguousarray(case.slots_h)]
-    if w["page_table"] is not None:
-        in_parts.append(np.ascontiguousarray(w["page_table"]))
-    in_offs, in_n = packed(in_parts)
-    h_in = torch.empty(in_n, dtype=torch.uint8).pin_memory()
-    for a, off in zip(in_parts, in_offs):
-        h_in[off:off + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
-    d_in = torch.empty(in_n, dtype=torch.uint8, device=dev)
-
-    def view(buf, off, a_shape, dtype):
-        n = int(np.prod(a_shape)) * torch.empty(0, dtype=dtype).element_size()
-        return buf[off:off + n].view(dtype).view(*a_shape)
-
-    q_e = view(d_in, in_offs[0], w["q_bf16"].shape, torch.bfloat16)
-    topk_e = view(d_in, in_offs[1], w["topk"].shape, torch.int32)
-    x_e = view(d_in, in_offs[2], case.x_new_h.shape, torch.bfloat16)
-    slots_e = view(d_in, in_offs[3], case.slots_h.shape, torch.int64)
-    pt_e = None if w["page_table"] is None else view(d_in, in_offs[4], w["page_table"].shape, torch.int32)
-    (o_off, lse_off), out_n = packed([np.empty((T, H, 512), np.uint16), np.empty((T, H), np.float32)])
-    d_out = torch.empty(out_n, dtype=torch.uint8, device=dev)
-    h_out = torch.empty(out_n, dtype=torch.uint8).pin_memory()
-    o_e = view(d_out, o_off, (T, H, 512), torch.bfloat16)
-    lse_e = view(d_out, lse_off, (T, H), torch.float32)
-    if prefill:
-        q8_e = torch.empty(T, H, 512, dtype=torch.uint8, device=dev)
-        qs_e = torch.empty(T, H, dtype=torch.float32, device=dev)
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
-    for i in range(n_e2e + 3):
-        timer.flush()
-        if i >= 3:
-            e2e_ev[i - 3][0].record(stream)
-        d_in.copy_(h_in, non_blocking=True)
-        case.writer(x_e, slots_e, case.pool)
-        if prefill:
-            binding.dsa_quantize_q8(q_e, q8_e, qs_e)
-            binding.dsa_sparse_attn_prefill_q8(q8_e, qs_e, case.pool, layout, topk_e, w["sm_scale"], o_e, lse_e,
-                                               case.ws, page_table=pt_e, page_size=w["page_size"])
-        else:
-            binding.dsa_sparse_attn_decode(q_e, case.pool, layout, topk_e, w["sm_scale"], o_e, lse_e, case.ws,
-                                           page_table=pt_e, page_size=w["page_size"])
-        h_out.copy_(d_out, non_blocking=True)
-        if i >= 3:
-            e2e_ev[i - 3][1].record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(float(sum(e[0].elapsed_time(e[1]) for e in e2e_ev)), dist, dev)
-    del d_in, h_in, d_out, h_out
+    # end to end through the public API, host buffers in and out
+    e2e_ms, n_e2e, in_n, out_n, e2e_flush = run_e2e(case, w, binding, dev, max(1, min(args.e2e_steps, args.steps)),
+                                                    timer)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     if rank != 0:
         return None
@@ -608,7 +554,12 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "e2e": {"value": round(world * T * n_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
-                "h2d_bytes_per_step": in_n, "d2h_bytes_per_step": out_n},
+                "h2d_bytes_per_step": in_n, "d2h_bytes_per_step": out_n,
+                "how": f"{n_e2e} steps through the C ABI from pinned host memory, pipelined over three "
+                       "streams (inputs of step i+1 uploading and outputs of step i-1 downloading while "
+                       "step i computes; two device buffer sets); "
+                       + ("L2 flushed before each step's kernels (inside the timed region)" if e2e_flush else
+                          f"no L2 flush: each step copies {(in_n + out_n) >> 20} MiB, more than L2")},
         "gpu_launches": case.launches_per_step() * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "fp8_peak": fp8,
@@ -619,6 +570,107 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
         line["per_config"] = run_per_config(args, dev, binding, timer, peaks, tpeak, tsrc,
                                             headline=(args.workload, roof, value))
     return line, w
+
+
+def run_e2e(case, w, binding, dev, n_steps: int, timer):
+    """End to end through the public API: every step copies its inputs (queries,
+    top-k lists, the new latent rows, their slots, the page table) from one
+    pinned host buffer to the device, runs writer (+ quantiser) + attention on
+    them, and copies O and LSE back to pinned host memory.  Steps are pipelined
+    over three streams with two device buffer sets: the upload of step i+1 and
+    the download of step i-1 overlap the kernels of step i.  Returns the summed
+    milliseconds of n_steps steps (first upload to last download), the steps,
+    the bytes copied per step each way, and whether L2 was flushed before each
+    step (when a step copies less than L2 holds)."""
+    import torch
+    T, H = w["T"], w["H"]
+
+    def packed(parts):
+        """Byte offsets of 256-byte-aligned parts in one buffer, and its size."""
+        offs, n = [], 0
+        for a in parts:
+            offs.append(n)
+            n += (a.nbytes + 255) // 256 * 256
+        return offs, n
+
+    in_parts = [np.ascontiguousarray(w["q_bf16"]), np.ascontiguousarray(w["topk"]),
+                np.ascontiguousarray(case.x_new_h), np.ascontiguousarray(case.slots_h)]
+    if w["page_table"] is not None:
+        in_parts.append(np.ascontiguousarray(w["page_table"]))
+    in_offs, in_n = packed(in_parts)
+    h_in = torch.empty(in_n, dtype=torch.uint8).pin_memory()
+    for a, off in zip(in_parts, in_offs):
+        h_in[off:off + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
+    (o_off, lse_off), out_n = packed([np.empty((T, H, 512), np.uint16), np.empty((T, H), np.float32)])
+
+    def view(buf, off, a_shape, dtype):
+        n = int(np.prod(a_shape)) * torch.empty(0, dtype=dtype).element_size()
+        return buf[off:off + n].view(dtype).view(*a_shape)
+
+    sets = []
+    for _ in range(2):
+        d_in = torch.empty(in_n, dtype=torch.uint8, device=dev)
+        d_out = torch.empty(out_n, dtype=torch.uint8, device=dev)
+        sets.append({
+            "d_in": d_in, "d_out": d_out, "h_out": torch.empty(out_n, dtype=torch.uint8).pin_memory(),
+            "q": view(d_in, in_offs[0], w["q_bf16"].shape, torch.bfloat16),
+            "topk": view(d_in, in_offs[1], w["topk"].shape, torch.int32),
+            "x": view(d_in, in_offs[2], case.x_new_h.shape, torch.bfloat16),
+            "slots": view(d_in, in_offs[3], case.slots_h.shape, torch.int64),
+            "pt": None if w["page_table"] is None else view(d_in, in_offs[4], w["page_table"].shape, torch.int32),
+            "o": view(d_out, o_off, (T, H, 512), torch.bfloat16),
+            "lse": view(d_out, lse_off, (T, H), torch.float32)})
+    if case.prefill:
+        q8 = torch.empty(T, H, 512, dtype=torch.uint8, device=dev)
+        qs = torch.empty(T, H, dtype=torch.float32, device=dev)
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    flush_each = (in_n + out_n) < torch.cuda.get_device_properties(dev).L2_cache_size and not timer.warm
+
+    def pipeline(n: int):
+        ev = [{k: torch.cuda.Event() for k in ("in", "comp", "out")} for _ in range(n)]
+        for i in range(n):
+            b = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev[i - 2]["comp"])          # the kernels of step i-2 read this set
+                b["d_in"].copy_(h_in, non_blocking=True)
+                ev[i]["in"].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev[i]["in"])
+                if i >= 2:
+                    s_comp.wait_event(ev[i - 2]["out"])         # step i-2's outputs have left this set
+                if flush_each:
+                    timer.flush()
+                case.writer(b["x"], b["slots"], case.pool)
+                if case.prefill:
+                    binding.dsa_quantize_q8(b["q"], q8, qs)
+                    binding.dsa_sparse_attn_prefill_q8(q8, qs, case.pool, case.layout, b["topk"], w["sm_scale"],
+                                                       b["o"], b["lse"], case.ws, page_table=b["pt"],
+                                                       page_size=w["page_size"])
+                else:
+                    binding.dsa_sparse_attn_decode(b["q"], case.pool, case.layout, b["topk"], w["sm_scale"],
+                                                   b["o"], b["lse"], case.ws, page_table=b["pt"],
+                                                   page_size=w["page_size"])
+                ev[i]["comp"].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev[i]["comp"])
+                b["h_out"].copy_(b["d_out"], non_blocking=True)
+                ev[i]["out"].record(s_out)
+        return ev
+
+    torch.cuda.synchronize(dev)
+    pipeline(3)                                                  # warm-up
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    ev = pipeline(n_steps)
+    for e in ev:                                                 # end after every step's download
+        s_out.wait_event(e["out"])
+    end.record(s_out)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end)
+    del sets, h_in
+    return ms, n_steps, in_n, out_n, flush_each
 
 
 def run_per_config(args, dev, binding, timer, peaks, tpeak, tsrc, headline) -> dict:
