@@ -194,18 +194,48 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(key: str):
-    """DRAM bytes per attention call from a committed ncu summary, only while the
-    kernel source is the one that was profiled."""
+def recorded_profile(key: str) -> dict | None:
+    """The committed ncu counters of one attention call (profiles/ncu_traffic.json),
+    only while the kernel source is the one that was profiled."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    if not os.path.exists(path):
+    if not key or not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
     e = rec.get(key)
     if not e or e.get("source_sha") != kernel_source_sha():
         return None
-    return e.get("dram_bytes_per_call")
+    return e
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes per attention call from the committed ncu counters."""
+    e = recorded_profile(key)
+    return e.get("dram_bytes_per_call") if e else None
+
+
+def torch_sms(dev) -> int:
+    import torch
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
+SMEM_BYTES_PER_CLK = 128     # shared-memory banks of one SM: 32 x 4 bytes a clock
+
+
+def smem_roofline(key: str, us: float, peaks: dict, sms: int) -> dict | None:
+    """Shared-memory bank traffic of one attention call (ncu l1tex__data_bank_reads
+    + _writes, 4 bytes each, recorded per kernel source) against 128 B a clock on
+    every SM at the maximum SM clock."""
+    e = recorded_profile(key)
+    if not e or "smem_bank_bytes_per_call" not in e:
+        return None
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = SMEM_BYTES_PER_CLK * sms * mhz * 1e6 / 1e9
+    b = e["smem_bank_bytes_per_call"]
+    gbs = b / (us * 1e-6) / 1e9
+    return {"achieved": round(gbs, 1), "peak": round(peak, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "bytes_per_call": b,
+            "peak_source": f"{SMEM_BYTES_PER_CLK} B/clk x {sms} SMs x {mhz:.0f} MHz (maximum SM clock)"}
 
 
 # -------------------------------------------------------------------- peaks
@@ -397,7 +427,7 @@ class AttnCase:
         return 1 + (1 if self.prefill else 0) + 1 + (1 if self.ws is not None else 0)
 
 
-def attn_roofline(w: dict, us: float, peaks: dict, tpeak: float, tsrc: str, traffic) -> dict:
+def attn_roofline(w: dict, us: float, peaks: dict, tpeak: float, tsrc: str, traffic, smem=None) -> dict:
     """Both rooflines of one attention call; `bound` names the binding one: HBM
     for the decode batches, the tensor pipe for the prefill batches (their pools
     sit in L2, so algorithmic HBM bytes there overstate what DRAM must move)."""
@@ -415,7 +445,8 @@ def attn_roofline(w: dict, us: float, peaks: dict, tpeak: float, tsrc: str, traf
             "hbm": {"achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
             "tensor": {"achieved": round(tfl, 2), "peak": tpeak, "unit": "TFLOP/s",
-                       "frac": round(tfl / tpeak, 4), "peak_source": tsrc}}
+                       "frac": round(tfl / tpeak, 4), "peak_source": tsrc},
+            **({"smem": smem} if smem else {})}
 
 
 def per_config_attention(key, w, dev, binding, timer, args, peaks, tpeak, tsrc) -> dict:
@@ -423,7 +454,8 @@ def per_config_attention(key, w, dev, binding, timer, args, peaks, tpeak, tsrc) 
     steps = max(5, min(args.steps, 20))
     us, runs = timer.median_call_us(case.attn, steps, args.warmup)
     step_ms = timer.run(case.step, steps)
-    roof = attn_roofline(w, us, peaks, tpeak, tsrc, recorded_traffic(key))
+    sms = torch_sms(dev)
+    roof = attn_roofline(w, us, peaks, tpeak, tsrc, recorded_traffic(key), smem_roofline(key, us, peaks, sms))
     return {"value": round(w["T"] * len(step_ms) / (sum(step_ms) / 1e3), 1), "unit": UNIT,
             "workload": w["name"], "T": w["T"], "H": w["H"], "K": w["K"], "layout": w["layout"],
             "pool_rows": w["pool_rows"], "valid_entries": W.valid_entry_count(w["topk"]),
@@ -534,8 +566,9 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist):
     peaks = measured_peaks()
     fp8 = measure_fp8_peak(dev)
     tpeak, tsrc = tensor_peak(peaks, fp8)
-    traffic = recorded_traffic(args.workload if args.workload != "writer_sweep" else None)
-    roof = attn_roofline(w, attn_us, peaks, tpeak, tsrc, traffic)
+    pkey = args.workload if args.workload != "writer_sweep" else None
+    roof = attn_roofline(w, attn_us, peaks, tpeak, tsrc, recorded_traffic(pkey),
+                         smem_roofline(pkey, attn_us, peaks, torch_sms(dev)))
     roof["attn_us_runs"] = attn_runs
     value = world * T * args.steps / (total_ms / 1e3)
     line = {
