@@ -130,6 +130,12 @@ static_assert(offsetof(Misc, ring) % 16 == 0 && offsetof(Misc, qsig) % 16 == 0, 
 template <int HG, bool kScaled, bool kQ8, bool kRope>
 struct Cfg {
   static constexpr int HPT = HG / 4;                           // heads per softmax thread
+  // P (and O) column order: with 8 heads a thread and unscaled rows, its
+  // three terms are 24 adjacent columns (head quarter q: columns 24 q + 8 term
+  // + head % 8), so a row of P goes out in one 16-byte and one 8-byte store;
+  // otherwise column term * HG + head (measured: the interleaved order saved
+  // 1.4 % on the FP8-query prefill and cost 0.6-1.8 % on 528-byte rows)
+  static constexpr bool kPInter = HPT == 8 && !kScaled;
   static constexpr int G = kScaled ? 4 : 1;                    // score accumulators per tile
   static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : 2 * HG;  // QK^T N (query operand rows)
   static constexpr int NP = (3 * HG + 15) / 16 * 16;          // PV N: P hi, mid, lo rows (+ zero pad)
@@ -856,6 +862,8 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   const int quarter = warp & 3, hq = warp >> 2;         // TMEM lane quarter, head quarter
   const int row = 32 * quarter + lane;                    // tile row = TMEM lane
   const int hbase = hq * HPT;                             // first head of this thread
+  // P / O column of this thread's first head in term t (0 hi, 1 mid, 2 lo)
+  auto tcol = [&](int t) { return C::kPInter ? hq * 24 + t * 8 : t * HG + hbase; };
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
   volatile int* abort = &ms.abort;
   float m_run[HPT], l_part[HPT];
@@ -1023,7 +1031,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
       for (int db = 0; db < 4; ++db) {
 #pragma unroll
         for (int term = 0; term < 3; ++term) {
-          const uint32_t ca = lane_base + C::O_COL0 + db * C::NP + term * HG + hbase;
+          const uint32_t ca = lane_base + C::O_COL0 + db * C::NP + tcol(term);
           uint32_t v[HPT];
           tmem_ld_cols<HPT>(ca, v);
           tmem_wait_ld();
@@ -1049,25 +1057,44 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     auto split = [](float v0, float v1, uint32_t& hi2, uint32_t& mid2, uint32_t& lo2) {
       split3_f16(v0, v1, hi2, mid2, lo2);
     };
-    // one term's HPT bytes of this row (P columns term * HG + hbase ..) in one
-    // store: they are consecutive in the MN-major operand
-    auto store_term = [&](uint32_t pg, int term, const uint32_t (&t2)[HPT / 2]) {
-      const uint32_t addr = pg + p_off<C::NP>(term * HG + hbase, row);
-      if constexpr (HPT == 8)
-        st_shared_v2(addr, t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16));
-      else if constexpr (HPT == 4)
-        st_shared_u32(addr, t2[0] | (t2[1] << 16));
-      else
-        st_shared_u16(addr, t2[0]);
+    // this row's P bytes: one term's HPT bytes are consecutive in the MN-major
+    // operand; with the interleaved order all three terms' 24 bytes are, and
+    // they go out as 16 + 8 bytes (even head quarter) or 8 + 16 (odd)
+    auto store_p = [&](uint32_t pg, const uint32_t (&hi2)[HPT / 2], const uint32_t (&mid2)[HPT / 2],
+                       const uint32_t (&lo2)[HPT / 2]) {
+      if constexpr (C::kPInter) {
+        const int n0 = hq * 24;
+        const uint32_t w0 = hi2[0] | (hi2[1] << 16), w1 = hi2[2] | (hi2[3] << 16);
+        const uint32_t w2 = mid2[0] | (mid2[1] << 16), w3 = mid2[2] | (mid2[3] << 16);
+        const uint32_t w4 = lo2[0] | (lo2[1] << 16), w5 = lo2[2] | (lo2[3] << 16);
+        if ((hq & 1) == 0) {
+          st_shared_v4(pg + p_off<C::NP>(n0, row), w0, w1, w2, w3);
+          st_shared_v2(pg + p_off<C::NP>(n0 + 16, row), w4, w5);
+        } else {
+          st_shared_v2(pg + p_off<C::NP>(n0, row), w0, w1);
+          st_shared_v4(pg + p_off<C::NP>(n0 + 8, row), w2, w3, w4, w5);
+        }
+      } else {
+        auto store_term = [&](int term, const uint32_t (&t2)[HPT / 2]) {
+          const uint32_t addr = pg + p_off<C::NP>(tcol(term), row);
+          if constexpr (HPT == 8)
+            st_shared_v2(addr, t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16));
+          else if constexpr (HPT == 4)
+            st_shared_u32(addr, t2[0] | (t2[1] << 16));
+          else
+            st_shared_u16(addr, t2[0]);
+        };
+        store_term(0, hi2);
+        store_term(1, mid2);
+        store_term(2, lo2);
+      }
     };
     if constexpr (kLateWait) {
       uint32_t hi2[HPT / 2], mid2[HPT / 2], lo2[HPT / 2];
 #pragma unroll
       for (int h = 0; h < HPT; h += 2) split(s2[h], s2[h + 1], hi2[h / 2], mid2[h / 2], lo2[h / 2]);
       if (it >= 1) ok &= mbar_wait(smem_u32(&ms.pv_done[0]), (it - 1) & 1, abort, a.wait_ns);
-      store_term(pbuf, 0, hi2);
-      store_term(pbuf, 1, mid2);
-      store_term(pbuf, 2, lo2);
+      store_p(pbuf, hi2, mid2, lo2);
     } else {
 #pragma unroll
       for (int g = 0; g < C::G; ++g) {
@@ -1076,9 +1103,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
         uint32_t hi2[HPT / 2], mid2[HPT / 2], lo2[HPT / 2];
 #pragma unroll
         for (int h = 0; h < HPT; h += 2) split(s2[h] * mul, s2[h + 1] * mul, hi2[h / 2], mid2[h / 2], lo2[h / 2]);
-        store_term(pg, 0, hi2);
-        store_term(pg, 1, mid2);
-        store_term(pg, 2, lo2);
+        store_p(pg, hi2, mid2, lo2);
       }
     }
     fence_proxy_async_smem();
@@ -1120,10 +1145,10 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
       for (int c0 = 0; c0 < HPT; c0 += kCh) {
         uint32_t hi[kCh], mid[kCh], lo[kCh];
-        const uint32_t ob = lane_base + C::O_COL0 + db * C::NP + hbase + c0;
-        tmem_ld_cols<kCh>(ob, hi);
-        tmem_ld_cols<kCh>(ob + HG, mid);
-        tmem_ld_cols<kCh>(ob + 2 * HG, lo);
+        const uint32_t ob = lane_base + C::O_COL0 + db * C::NP + c0;
+        tmem_ld_cols<kCh>(ob + tcol(0), hi);
+        tmem_ld_cols<kCh>(ob + tcol(1), mid);
+        tmem_ld_cols<kCh>(ob + tcol(2), lo);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < kCh; ++k) {
