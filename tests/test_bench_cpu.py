@@ -82,6 +82,24 @@ def test_tensor_peak_choice():
     assert bench.tensor_peak({}, None)[0] == 2 * bench.FALLBACK_BF16_TFLOPS
 
 
+def test_recorded_counters_follow_the_kernel_source(monkeypatch):
+    """The DRAM and shared-memory figures of the ncu record are used only while
+    the kernel source hashes to the profiled one; the bank roofline is bytes /
+    time against 128 B a clock on every SM."""
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        rec = json.load(f)
+    e = rec["prefill_q8_raw512"]
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda: e["source_sha"])
+    assert bench.recorded_traffic("prefill_q8_raw512") == e["dram_bytes_per_call"]
+    r = bench.smem_roofline("prefill_q8_raw512", 1000.0, {"sm_max_mhz": 2000.0}, 100)
+    assert r["peak"] == 128 * 100 * 2000e6 / 1e9
+    assert abs(r["achieved"] - e["smem_bank_bytes_per_call"] / 1e-3 / 1e9) < 0.1
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-4
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda: "0" * 16)
+    assert bench.recorded_traffic("prefill_q8_raw512") is None
+    assert bench.smem_roofline("prefill_q8_raw512", 1000.0, {}, 100) is None
+
+
 def test_reference_arm_line():
     """The reference arm times the oracle on the host cores and prints one JSON line
     with the metric, the impl tag, a cpu_baseline and an e2e with no copies."""
