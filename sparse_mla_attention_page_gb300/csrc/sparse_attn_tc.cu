@@ -137,7 +137,11 @@ struct Cfg {
   // 1.4 % on the FP8-query prefill and cost 0.6-1.8 % on 528-byte rows)
   static constexpr bool kPInter = HPT == 8 && !kScaled;
   static constexpr int G = kScaled ? 4 : 1;                    // score accumulators per tile
-  static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : 2 * HG;  // QK^T N (query operand rows)
+  // BF16 queries over 528-byte rows at 32 heads: the hi and lo halves of the
+  // query are two K ranges of one N = HG operand (S = K.hi + K.lo in one
+  // accumulator), not 2 HG columns, so that two groups' scores share a chunk
+  static constexpr bool kHalvesK = kScaled && !kQ8 && !kRope && HG == 32;
+  static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : kHalvesK ? HG : 2 * HG;  // QK^T N (query operand rows)
   static constexpr int NP = (3 * HG + 15) / 16 * 16;          // PV N: P hi, mid, lo rows (+ zero pad)
   static constexpr int O_COLS = 4 * NP;
   // 656-byte rows: the RoPE part of the scores, S_rope = K_rope Q_rope^T (BF16
@@ -158,7 +162,7 @@ struct Cfg {
   static constexpr int USED = O_COL0 + O_COLS;
   static constexpr int TMEM_COLS =
       USED <= 32 ? 32 : USED <= 64 ? 64 : USED <= 128 ? 128 : USED <= 256 ? 256 : 512;
-  static constexpr int Q_BYTES = NQ * 512;
+  static constexpr int Q_BYTES = NQ * 512 * (kHalvesK ? 2 : 1);
   static constexpr int P_BYTES = G * NP * 128;
   static constexpr int ROPE_STAGE = kRope ? kRows * 128 : 0;   // RoPE parts of a tile: 128 rows x 128 B
   static constexpr int QR_BYTES = NR * 128;                    // RoPE query operand
@@ -340,9 +344,12 @@ struct TileCursor {
 // 128-byte swizzle, and the log2-domain multiplier of each score column.
 // BF16 queries: rows [hi heads | lo heads], the exact two-term FP8 split
 // hi = e4m3(q 2^sh), lo = e4m3((q 2^sh - hi) 16) with a power of two 2^sh per
-// head.  FP8 queries: the bytes as they are, multiplier q_scale (rows past HG
+// head; with kHalvesK the rows are the heads and lo = e4m3(q 2^sh - hi) sits
+// at K offset 512 of the same row (exact while the residual is an E4M3
+// normal, for elements within about 2^10 of the head's amax; smaller ones
+// keep fewer bits, below 2^-18 of the amax).  FP8 queries: the bytes as they are, multiplier q_scale (rows past HG
 // stay zero).  Thread -> head tid / TPH, dims [DPT (tid % TPH), + DPT).
-template <int HG, bool kQ8, bool kRope>
+template <int HG, bool kQ8, bool kRope, bool kHalvesK>
 struct QueryBuild {
   static constexpr int kThr = kSmxThreads < 32 * HG ? kSmxThreads : 32 * HG;   // threads that build
   static constexpr int TPH = kThr / HG;                   // threads per head (one warp at most)
@@ -425,17 +432,20 @@ struct QueryBuild {
             hi[i] = e4m3x4_satrne(y[0], y[1], y[2], y[3]);
             e4m3x4_to_f32(hi[i], yh);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) r[j] = (y[j] - yh[j]) * 16.f;
+            for (int j = 0; j < 4; ++j) r[j] = kHalvesK ? y[j] - yh[j] : (y[j] - yh[j]) * 16.f;
             lo[i] = e4m3x4_satrne(r[0], r[1], r[2], r[3]);
           }
         }
         const int k0 = part * DPT + 16 * c;
         *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(head, k0)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(HG + head, k0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if constexpr (kHalvesK)   // lo = q 2^sh - hi at K offset 512 of the same row
+          *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(head, kD + k0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        else
+          *reinterpret_cast<uint4*>(qbuf + kmajor_off<NQ>(HG + head, k0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       if (part == 0) {
         qsig[head] = sig;
-        qsig[HG + head] = sig * 0.0625f;
+        if constexpr (!kHalvesK) qsig[HG + head] = sig * 0.0625f;
       }
     }
   }
@@ -776,6 +786,9 @@ __device__ void qk_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t tmem,
         const uint64_t bd = desc_add(bd0, kb * (C::NQ * 128) + kk * 32);
         // 528-byte rows: one accumulator per group (scaled by its rows' scales later)
         mma_e4m3(d_base + (kScaled ? kb * C::NQ : 0), ad, bd, kIdQK, (kScaled ? kk > 0 : st > 0) ? 1u : 0u);
+        // the query's lo half: K offset 512 of the same rows, same accumulator
+        if constexpr (C::kHalvesK)
+          mma_e4m3(d_base + kb * C::NQ, ad, desc_add(bd, 4 * (C::NQ * 128)), kIdQK, 1u);
       }
       if (kRope && qc == 0) {
         // S_rope = K_rope Q_rope^T: 64 BF16 dims, K = 16 per MMA
@@ -873,7 +886,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   int seg = -1;
   bool ok = true;                  // false once a wait gave up: keep going through every barrier
   TileCursor cur(a, b0);
-  QueryBuild<HG, kQ8, kRope> qnext;   // the next segment's query, loaded ahead of its build
+  QueryBuild<HG, kQ8, kRope, C::kHalvesK> qnext;   // the next segment's query, loaded ahead of its build
   qnext.load(a, cur.t, cur.hgi * a.hg);
   qnext.template store<C::NQ>(a, sm + C::Q_OFF, ms.qsig[0], sm + C::QR_OFF);
   fence_proxy_async_smem();
@@ -919,14 +932,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
         const uint32_t cbase = lane_base + sb * C::S_COLS + gl * C::NQ;
         uint32_t hi[HPT], lo[HPT];
         tmem_ld_cols<HPT>(cbase + hbase, hi);
-        if (!kQ8) tmem_ld_cols<HPT>(cbase + HG + hbase, lo);
+        if (!kQ8 && !C::kHalvesK) tmem_ld_cols<HPT>(cbase + HG + hbase, lo);
         tmem_wait_ld();
         float qs_hi[HPT], qs_lo[HPT];   // score column multipliers (16-byte aligned runs)
 #pragma unroll
         for (int k = 0; k < HPT; k += 4) {
           const float4 m4 = *reinterpret_cast<const float4*>(&ms.qsig[qb][hbase + k]);
           qs_hi[k] = m4.x; qs_hi[k + 1] = m4.y; qs_hi[k + 2] = m4.z; qs_hi[k + 3] = m4.w;
-          if (!kQ8) {
+          if (!kQ8 && !C::kHalvesK) {
             const float4 l4 = *reinterpret_cast<const float4*>(&ms.qsig[qb][HG + hbase + k]);
             qs_lo[k] = l4.x; qs_lo[k + 1] = l4.y; qs_lo[k + 2] = l4.z; qs_lo[k + 3] = l4.w;
           }
@@ -934,7 +947,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
         for (int k = 0; k < HPT; ++k) {
           float v = __uint_as_float(hi[k]) * qs_hi[k];
-          if (!kQ8) v = fmaf(__uint_as_float(lo[k]), qs_lo[k], v);
+          if (!kQ8 && !C::kHalvesK) v = fmaf(__uint_as_float(lo[k]), qs_lo[k], v);
           s2[k] = kScaled ? fmaf(sc4[g], v, s2[k]) : v;
         }
       }
