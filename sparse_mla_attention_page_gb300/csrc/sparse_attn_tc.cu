@@ -4,7 +4,7 @@
 // of the global work list (unit = token x group of HG <= 32 heads; a unit's
 // top-k list is tpt tiles).  Consecutive tiles of one unit form a segment;
 // each segment ends with an epilogue that writes the unit's O and LSE (or a
-// partial result when the unit spans CTAs).  Warp roles:
+// partial result when the unit spans CTAs).  Warp roles (24 warps):
 //
 //   index      1 warp: translates each tile's 128 top-k entries through the
 //              page table into physical rows (top-k entries fetched three
@@ -12,7 +12,7 @@
 //              latency sits between tiles), publishes them in a ring of
 //              kRing tiles for the producers; nothing ties it to the stages,
 //              so it runs up to kRing tiles ahead of them.
-//   producer   2 warps: publish a stage's valid-entry bits once the stage is
+//   producer   5 warps: publish a stage's valid-entry bits once the stage is
 //              free, then gather each tile's rows with 16-byte cp.async into
 //              the 128-byte-swizzled K-major tile, four rows x 128 bytes per
 //              warp instruction (whole 128-byte lines), zero-filling masked
@@ -22,30 +22,27 @@
 //              (cp.async.mbarrier.arrive.noinc).  (Row gathers through the
 //              tensor memory accelerator, tile::gather4, are issue-bound and
 //              ran slower than cp.async here.)
-//   MMA        1 thread: S^T = K Q^T (M = 128 rows, N = query columns, K = 512)
-//              and O^T += V^T P^T (M = 128 latent dims x 4, N = P columns,
-//              K = 128 rows), both kind::f8f6f4 with FP32 accumulators in
-//              tensor memory, issued in whatever order their inputs become
-//              ready (one MMA of K=32 occupies the tensor pipe for the same
-//              ~64 cycles for any N up to 128, so the pipe must never wait on
-//              one queue while the other is ready).  The same shared-memory
-//              tile is the K-major A operand of the first and the MN-major A operand
-//              of the second (V = K: one absorbed NoPE latent row).  Over
-//              656-byte rows, four kind::f16 MMAs per tile add the BF16 RoPE
-//              scores K_rope Q_rope^T in extra score columns.
-//   softmax    8 warps, two per TMEM lane quarter, each thread one tile row
-//              (= TMEM lane) and half of the heads: combine the score
+//   QK^T       1 thread: S^T = K Q^T (M = 128 rows, N = query columns,
+//              K = 512) per score chunk, kind::f8f6f4 with FP32 accumulators
+//              in tensor memory; over 656-byte rows four kind::f16 MMAs per
+//              tile add the BF16 RoPE scores K_rope Q_rope^T in extra columns.
+//   PV         1 thread: O^T += V^T P^T (M = 128 latent dims x 4, N = P
+//              columns, K = 128 rows).  The same shared-memory tile is the
+//              K-major A operand of QK^T and the MN-major A operand of PV
+//              (V = K: one absorbed NoPE latent row).  Two issuing threads
+//              keep the tensor pipe fed while either one waits for its inputs.
+//   softmax    16 warps, four per TMEM lane quarter, each thread one tile row
+//              (= TMEM lane) and a quarter of the heads: combine the score
 //              columns, mask, keep a lazy running max (one barrier with an
 //              OR reduction asks whether any row exceeds its head's running
 //              max by more than 2^8; only then are the per-head tile maxima
 //              across the 128 rows formed and O in TMEM rescaled; 528-byte
 //              rows, which also track the group-scale exponents, form them
-//              every tile), form p = 2^(s - m),
-//              accumulate the denominators, write P as an FP8 operand, build
-//              each segment's query operand in shared memory (loads issued a
-//              tile ahead), and at the end of a segment normalise O and store
-//              it (a unit whose
-//              tiles span CTAs leaves a normalised partial O and LSE per CTA;
+//              every tile), form p = 2^(s - m), accumulate the denominators,
+//              write P as an FP8 operand, build each segment's query operand
+//              in shared memory (loads issued a tile ahead), and at the end of
+//              a segment normalise O and store it (a unit whose tiles span
+//              CTAs leaves a normalised partial O and LSE per CTA;
 //              combine_kernel, launched right behind as a programmatic
 //              dependent, merges them).
 //
