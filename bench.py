@@ -45,9 +45,12 @@ METRIC = "sparse-attn query-tokens/s and KV-gather HBM GB/s (fraction of GB300 r
 UNIT = "query-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# the sources of the profiled kernel (ncu -k regex:sparse_attn_tc): its recorded
+# counters stay valid while these hash the same
 ATTN_SOURCES = ["sparse_mla_attention_page_gb300/csrc/sparse_attn_tc.cu",
                 "sparse_mla_attention_page_gb300/csrc/tc_ptx.cuh",
-                "sparse_mla_attention_page_gb300/csrc/combine.cu"]
+                "sparse_mla_attention_page_gb300/csrc/dsa_common.cuh",
+                "sparse_mla_attention_page_gb300/csrc/kernels.h"]
 ATTN_KERNEL = "sparse_attn_tc_kernel + combine_kernel (the attention call)"
 COMPUTE_DTYPE = "e4m3"         # tcgen05 kind::f8f6f4 MMAs (E4M3 operands, FP32 accumulation)
 RUNS = 5                       # runs per roofline figure (median of the runs' mean call time)

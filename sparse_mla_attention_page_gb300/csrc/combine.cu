@@ -20,14 +20,34 @@ constexpr int kThreads = 256;
 constexpr int kBatch = 4;            // parts whose loads are issued together
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
-  const int k = blockIdx.x + 1;
-  const int64_t bk = tile_begin(k, a.n_tiles, a.grid);
-  const int64_t u = bk / a.tpt;
-  const int64_t u0 = u * a.tpt;
-  if (bk == u0) return;                                              // a boundary between units
-  if (k >= 2 && tile_begin(k - 1, a.n_tiles, a.grid) > u0) return;   // merged at an earlier boundary
-  const int c0 = cta_of_tile(u0, a.n_tiles, a.grid);
-  const int c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
+  // The block's unit and parts, worked out once by one thread (64-bit
+  // divisions: issued by every thread they made the kernel instruction-bound).
+  __shared__ int64_t s_th0;                // output row of the unit's first head
+  __shared__ int s_c0, s_c1, s_slot0;      // s_c0 < 0: nothing to merge here
+  if (threadIdx.x == 0) {
+    const int k = blockIdx.x + 1;
+    const int64_t bk = tile_begin(k, a.n_tiles, a.grid);
+    const int64_t u0 = bk / a.tpt * a.tpt;
+    int c0 = -1, c1 = -1, slot0 = 0;
+    // a boundary inside a unit, and the first such boundary of that unit
+    if (bk != u0 && !(k >= 2 && tile_begin(k - 1, a.n_tiles, a.grid) > u0)) {
+      c0 = cta_of_tile(u0, a.n_tiles, a.grid);
+      c1 = cta_of_tile(u0 + a.tpt - 1, a.n_tiles, a.grid);
+      // slot 0 of a CTA holds the unit its range starts in, slot 1 its last
+      // unit: the unit is the last one of CTA c0 unless its range starts at u0,
+      // and the first one of every later CTA
+      slot0 = 2 * c0 + (tile_begin(c0, a.n_tiles, a.grid) < u0 ? 1 : 0);
+    }
+    const int64_t u = u0 / a.tpt;
+    const int t = (int)(u / a.hgs);
+    s_th0 = (int64_t)t * a.H + (int)(u - (int64_t)t * a.hgs) * a.hg;
+    s_c0 = c0;
+    s_c1 = c1;
+    s_slot0 = slot0;
+  }
+  __syncthreads();
+  const int c0 = s_c0, c1 = s_c1;
+  if (c0 < 0) return;
   const int item = blockIdx.y * kThreads + threadIdx.x;
   const int h = item / (kD / 4), d4 = item % (kD / 4);
   asm volatile("griddepcontrol.wait;" ::: "memory");               // every partial is written
@@ -42,8 +62,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
       ls[p] = -INFINITY;
       v[p] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c <= c1) {
-        // slot 0 of a CTA holds the unit its range starts in, slot 1 its last unit
-        const int64_t sb = ((int64_t)c * 2 + (tile_begin(c, a.n_tiles, a.grid) < u0 ? 1 : 0)) * a.hg + h;
+        const int64_t sb = (int64_t)(c == c0 ? s_slot0 : 2 * c) * a.hg + h;
         ls[p] = __ldcg(a.ws_lse + sb);
         v[p] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + sb * kD) + d4);
       }
@@ -67,8 +86,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
   uint2 packed;
   packed.x = *reinterpret_cast<uint32_t*>(&lo);
   packed.y = *reinterpret_cast<uint32_t*>(&hi);
-  const int t = (int)(u / a.hgs);
-  const int64_t th = (int64_t)t * a.H + (int)(u - (int64_t)t * a.hgs) * a.hg + h;
+  const int64_t th = s_th0 + h;
   reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + th * kD)[d4] = packed;
   if (d4 == 0) a.lse[th] = sum > 0.f ? m + logf(sum) : -INFINITY;
 }
