@@ -456,6 +456,18 @@ def per_config_attention(key, w, dev, binding, timer, args, peaks, tpeak, tsrc) 
     case = AttnCase(w, dev, binding)
     steps = max(5, min(args.steps, 20))
     us, runs = timer.median_call_us(case.attn, steps, args.warmup)
+    warm = None
+    if not is_prefill(w) and not timer.warm:
+        # second column: back-to-back calls with no flush, the pool staying in L2
+        # as far as it fits (informational; the cold figure is the roofline's)
+        timer.warm = True
+        try:
+            warm_us, _ = timer.median_call_us(case.attn, steps, args.warmup)
+        finally:
+            timer.warm = False
+        warm = {"attn_us_per_call": round(warm_us, 3),
+                "hbm_frac": round(algorithmic_bytes(w) / (warm_us * 1e-6) / 1e9
+                                  / float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)), 4)}
     step_ms = timer.run(case.step, steps)
     sms = torch_sms(dev)
     roof = attn_roofline(w, us, peaks, tpeak, tsrc, recorded_traffic(key), smem_roofline(key, us, peaks, sms))
@@ -463,7 +475,8 @@ def per_config_attention(key, w, dev, binding, timer, args, peaks, tpeak, tsrc) 
             "workload": w["name"], "T": w["T"], "H": w["H"], "K": w["K"], "layout": w["layout"],
             "pool_rows": w["pool_rows"], "valid_entries": W.valid_entry_count(w["topk"]),
             "attn_us_per_call": round(us, 3), "attn_us_runs": runs,
-            "step_us": round(statistics.mean(step_ms) * 1e3, 3), "roofline": roof}
+            "step_us": round(statistics.mean(step_ms) * 1e3, 3), "roofline": roof,
+            **({"warm": warm} if warm else {})}
 
 
 def per_config_kv_write(layout, dev, binding, timer, args, peaks) -> dict:
