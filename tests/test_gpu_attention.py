@@ -170,6 +170,28 @@ def test_peaked_softmax(layout):
     assert st["rel_to_max"] <= 1e-2, st
 
 
+@pytest.mark.parametrize("scale", [1.0, 4.0, 16.0])
+@pytest.mark.parametrize("peaked", [False, True])
+def test_prefill_q8_row_magnitudes(scale, peaked):
+    """FP8 queries over raw rows carry P in two E4M3 terms (relative error up to
+    2^-8 per entry, so the error of O grows with the rows' magnitudes): rows of
+    N(0, scale^2) latents (entries up to about 70 at scale 16), with a flat and
+    with a peaked softmax (queries scaled so the logits keep their spread), stay
+    within the tolerance at 32 heads."""
+    T, H, K = 8, 32, 1024
+    w = W.decode_raw512(seed=310, T=T, H=H, K=K, pool_rows=8192, special_tokens=False)
+    w["kv_src"] = W.f32_to_bf16_bits(W.bf16_bits_to_f32(w["kv_src"]) * np.float32(2.0 * scale))
+    if peaked:
+        w["q_bf16"] = W.f32_to_bf16_bits(W.bf16_bits_to_f32(w["q_bf16"]) * np.float32(100.0 / scale))
+    pool, pd = pool_for(w, ("magnitude", scale, peaked))
+    q8, qs = oracle.quantize_q8(w["q_bf16"])
+    O, L, err = run_prefill(w, pd, q8, qs)
+    Or, Lr, _ = oracle.sparse_attn(pool, "raw512", w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                                   page_table=w["page_table"])
+    assert err == 0
+    assert_attn_close(O, L, Or, Lr, f"q8 rows x{scale} {'peaked' if peaked else 'flat'}")
+
+
 def test_prefill_q8_short_context_padding():
     """Zero prior context: early tokens have fewer than K causal rows, so the
     list is padded with -1 (down to a single valid entry for the first token)."""
