@@ -46,13 +46,17 @@
 //              combine_kernel, launched right behind as a programmatic
 //              dependent, merges them).
 //
-// Exact FP8 operands for BF16 data: a BF16 query q is split per head into
+// FP8 operands for BF16 data: a BF16 query q is split per head into
 // hi = e4m3(q * 2^a) and lo = e4m3((q * 2^a - hi) * 16) with a power-of-two
-// 2^a; hi + lo/16 reproduces q * 2^a exactly (8 significant bits), so
-// S = K.hi + K.lo/16 loses nothing but FP32 accumulation order.  P is split
-// into three FP8 terms, p ~ hi + mid/16 + lo/256 (about 13 significant bits),
-// because the output is a softmax-weighted sum of rows whose entries can be
-// large while the sum cancels: two terms (8 bits) are not enough there.  For
+// 2^a placing the head's amax at the top of the E4M3 range; hi + lo/16
+// reproduces q * 2^a exactly (8 significant bits) for every element within
+// about 2^15 of the amax (smaller ones fall into the E4M3 subnormals and keep
+// fewer bits, below 2^-15 of the largest term), so S = K.hi + K.lo/16 loses
+// little beyond FP32 accumulation order.  P is split into three FP8 terms,
+// p ~ hi + mid/16 + lo/256 (the FP16 value of p, 11 significant bits), because
+// the output is a softmax-weighted sum of rows whose entries can be large
+// while the sum cancels; FP8 queries over unscaled rows use two terms (8
+// bits), measured within the tolerance there (Cfg::NTERMS).  For
 // 528-byte rows the four group scales enter S per row (one accumulator per
 // 128-dim group) and P per group (P_g = p * scale_g * 2^-E_g, E_g a running
 // power of two bounding the segment's scales), so value rows are never
@@ -360,15 +364,16 @@ struct TileCursor {
 // ------------------------------------------------------------ query operand
 
 // The QK^T B operand of one unit (token t, heads h0 .. h0 + HG - 1), built by
-// the 256 softmax threads straight into a query buffer: K-major with the
+// the softmax threads straight into a query buffer: K-major with the
 // 128-byte swizzle, and the log2-domain multiplier of each score column.
 // BF16 queries: rows [hi heads | lo heads], the exact two-term FP8 split
 // hi = e4m3(q 2^sh), lo = e4m3((q 2^sh - hi) 16) with a power of two 2^sh per
 // head; with kHalvesK the rows are the heads and lo = e4m3(q 2^sh - hi) sits
 // at K offset 512 of the same row (exact while the residual is an E4M3
 // normal, for elements within about 2^10 of the head's amax; smaller ones
-// keep fewer bits, below 2^-18 of the amax).  FP8 queries: the bytes as they are, multiplier q_scale (rows past HG
-// stay zero).  Thread -> head tid / TPH, dims [DPT (tid % TPH), + DPT).
+// keep fewer bits, below 2^-18 of the amax).  FP8 queries: the bytes as they
+// are, multiplier q_scale (rows past HG stay zero).  Thread -> head tid / TPH,
+// dims [DPT (tid % TPH), + DPT).
 template <int HG, bool kQ8, bool kRope, bool kHalvesK>
 struct QueryBuild {
   static constexpr int kThr = kSmxThreads < 32 * HG ? kSmxThreads : 32 * HG;   // threads that build
@@ -1282,8 +1287,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const __gri
   // of this grid exit and wait for the whole grid before reading partials
   grid_launch_dependents();
 
-  // 16 warps: softmax warpgroups 0-1 grow to SMX_REGS registers a thread, the
-  // MMA / index / producer warpgroups 2-3 shrink to OTHER_REGS
+  // 24 warps: the four softmax warpgroups (warps 0-15) grow to SMX_REGS
+  // registers a thread, the two others (MMA issuers, index, producers) shrink
+  // to OTHER_REGS
   static_assert(C::SMX_REGS % 8 == 0 && C::OTHER_REGS % 8 == 0 && C::SMX_REGS > kLaunchRegs &&
                 C::OTHER_REGS < kLaunchRegs && C::OTHER_REGS >= 24 &&
                 C::SMX_REGS * kSmxThreads + C::OTHER_REGS * (kThreads - kSmxThreads) == kLaunchRegs * kThreads,
