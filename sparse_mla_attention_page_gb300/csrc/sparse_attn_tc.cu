@@ -55,8 +55,8 @@
 // little beyond FP32 accumulation order.  P is split into three FP8 terms,
 // p ~ hi + mid/16 + lo/256 (the FP16 value of p, 11 significant bits), because
 // the output is a softmax-weighted sum of rows whose entries can be large
-// while the sum cancels; FP8 queries over unscaled rows use two terms (8
-// bits), measured within the tolerance there (Cfg::NTERMS).  For
+// while the sum cancels: two terms (8 bits, relative error up to 2^-8) broke
+// the tolerance once rows held entries beyond about 20 (measured).  For
 // 528-byte rows the four group scales enter S per row (one accumulator per
 // 128-dim group) and P per group (P_g = p * scale_g * 2^-E_g, E_g a running
 // power of two bounding the segment's scales), so value rows are never
@@ -143,15 +143,7 @@ struct Cfg {
   // accumulator), not 2 HG columns, so that two groups' scores share a chunk
   static constexpr bool kHalvesK = kScaled && !kQ8 && !kRope && HG == 32;
   static constexpr int NQ = kQ8 ? (HG < 16 ? 16 : HG) : kHalvesK ? HG : 2 * HG;  // QK^T N (query operand rows)
-  // P terms: three E4M3 terms (p ~ hi + mid/16 + lo/256, the FP16 value of p),
-  // or two (p ~ hi + mid/16, relative error at most 2^-8 + 2^-11) for FP8
-  // queries over unscaled rows.  Two terms bound the error of O by about
-  // 2^-8 max|V|: measured within the tolerance on the FP8-query cases over
-  // unscaled rows (the BF16 rounding of O dominates), but over group-scaled
-  // rows, whose values reach 10-20, cancelling sums broke it, so those keep
-  // three terms.
-  static constexpr int NTERMS = kQ8 && !kScaled ? 2 : 3;
-  static constexpr int NP = (NTERMS * HG + 15) / 16 * 16;     // PV N: P term rows (+ zero pad)
+  static constexpr int NP = (3 * HG + 15) / 16 * 16;          // PV N: P hi, mid, lo rows (+ zero pad)
   static constexpr int O_COLS = 4 * NP;
   // 656-byte rows: the RoPE part of the scores, S_rope = K_rope Q_rope^T (BF16
   // MMAs, N = NR query rows), accumulated in NR more columns of each score buffer
@@ -260,21 +252,6 @@ __device__ __forceinline__ void split3_f16(float v0, float v1, uint32_t& hi2, ui
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r2) : "r"(r2), "r"(0x4C004C00u));
   asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(r2));
   lo2 = h;
-}
-
-// Two E4M3 terms of a pair of P values, v ~ hi + mid/16 (the first two terms
-// of split3_f16).
-__device__ __forceinline__ void split2_f16(float v0, float v1, uint32_t& hi2, uint32_t& mid2) {
-  uint32_t p, t, r;
-  uint16_t h;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p) : "f"(v1), "f"(v0));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(p));
-  hi2 = h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(t) : "h"(h));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(t));
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x4C004C00u));   // x 16
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(r));
-  mid2 = h;
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
@@ -901,7 +878,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
   const int row = 32 * quarter + lane;                    // tile row = TMEM lane
   const int hbase = hq * HPT;                             // first head of this thread
   // P / O column of this thread's first head in term t (0 hi, 1 mid, 2 lo)
-  auto tcol = [&](int t) { return C::kPInter ? hq * (8 * C::NTERMS) + t * 8 : t * HG + hbase; };
+  auto tcol = [&](int t) { return C::kPInter ? hq * 24 + t * 8 : t * HG + hbase; };
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
   volatile int* abort = &ms.abort;
   float m_run[HPT], l_part[HPT];
@@ -1068,7 +1045,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
 #pragma unroll
       for (int db = 0; db < 4; ++db) {
 #pragma unroll
-        for (int term = 0; term < C::NTERMS; ++term) {
+        for (int term = 0; term < 3; ++term) {
           const uint32_t ca = lane_base + C::O_COL0 + db * C::NP + tcol(term);
           uint32_t v[HPT];
           tmem_ld_cols<HPT>(ca, v);
@@ -1093,23 +1070,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
     }
     // three E4M3 terms of a pair of P values: v ~ hi + mid / 16 + lo / 256
     auto split = [](float v0, float v1, uint32_t& hi2, uint32_t& mid2, uint32_t& lo2) {
-      if constexpr (C::NTERMS == 3) {
-        split3_f16(v0, v1, hi2, mid2, lo2);
-      } else {
-        split2_f16(v0, v1, hi2, mid2);
-        lo2 = 0;
-      }
+      split3_f16(v0, v1, hi2, mid2, lo2);
     };
     // this row's P bytes: one term's HPT bytes are consecutive in the MN-major
     // operand; with the interleaved order all three terms' 24 bytes are, and
     // they go out as 16 + 8 bytes (even head quarter) or 8 + 16 (odd)
     auto store_p = [&](uint32_t pg, const uint32_t (&hi2)[HPT / 2], const uint32_t (&mid2)[HPT / 2],
                        const uint32_t (&lo2)[HPT / 2]) {
-      if constexpr (C::kPInter && C::NTERMS == 2) {   // [hi 8 | mid 8]: one 16-byte store
-        const uint32_t w0 = hi2[0] | (hi2[1] << 16), w1 = hi2[2] | (hi2[3] << 16);
-        const uint32_t w2 = mid2[0] | (mid2[1] << 16), w3 = mid2[2] | (mid2[3] << 16);
-        st_shared_v4(pg + p_off<C::NP>(hq * 16, row), w0, w1, w2, w3);
-      } else if constexpr (C::kPInter) {
+      if constexpr (C::kPInter) {
         const int n0 = hq * 24;
         const uint32_t w0 = hi2[0] | (hi2[1] << 16), w1 = hi2[2] | (hi2[3] << 16);
         const uint32_t w2 = mid2[0] | (mid2[1] << 16), w3 = mid2[2] | (mid2[3] << 16);
@@ -1133,7 +1101,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
         };
         store_term(0, hi2);
         store_term(1, mid2);
-        if constexpr (C::NTERMS == 3) store_term(2, lo2);
+        store_term(2, lo2);
       }
     };
     if constexpr (kLateWait) {
@@ -1195,14 +1163,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* sm, Misc& ms, uint32_t 
         const uint32_t ob = lane_base + C::O_COL0 + db * C::NP + c0;
         tmem_ld_cols<kCh>(ob + tcol(0), hi);
         tmem_ld_cols<kCh>(ob + tcol(1), mid);
-        if constexpr (C::NTERMS == 3) tmem_ld_cols<kCh>(ob + tcol(2), lo);
+        tmem_ld_cols<kCh>(ob + tcol(2), lo);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < kCh; ++k) {
           const int h = hbase + c0 + k;
           const float li = ms.linv[h];
-          const float lo_f = C::NTERMS == 3 ? __uint_as_float(lo[k]) : 0.f;
-          const float acc = fmaf(lo_f, 0.00390625f, fmaf(__uint_as_float(mid[k]), 0.0625f, __uint_as_float(hi[k])));
+          const float acc = fmaf(__uint_as_float(lo[k]), 0.00390625f,
+                                 fmaf(__uint_as_float(mid[k]), 0.0625f, __uint_as_float(hi[k])));
           const float o = li == 0.f ? 0.f : acc * pw2 * li;
           if (whole)
             static_cast<__nv_bfloat16*>(a.o)[((int64_t)cur.t * a.H + h0 + h) * kD + d] = __float2bfloat16_rn(o);

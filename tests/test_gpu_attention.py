@@ -173,11 +173,11 @@ def test_peaked_softmax(layout):
 @pytest.mark.parametrize("scale", [1.0, 4.0, 16.0])
 @pytest.mark.parametrize("peaked", [False, True])
 def test_prefill_q8_row_magnitudes(scale, peaked):
-    """FP8 queries over raw rows carry P in two E4M3 terms (relative error up to
-    2^-8 per entry, so the error of O grows with the rows' magnitudes): rows of
-    N(0, scale^2) latents (entries up to about 70 at scale 16), with a flat and
-    with a peaked softmax (queries scaled so the logits keep their spread), stay
-    within the tolerance at 32 heads."""
+    """The error of O from the FP8 split of P grows with the rows' magnitudes
+    (relative error of a P entry times max|V|): rows of N(0, scale^2) latents
+    (entries up to about 70 at scale 16), with a flat and with a peaked softmax
+    (queries scaled so the logits keep their spread), stay within the tolerance
+    at 32 heads with FP8 queries."""
     T, H, K = 8, 32, 1024
     w = W.decode_raw512(seed=310, T=T, H=H, K=K, pool_rows=8192, special_tokens=False)
     w["kv_src"] = W.f32_to_bf16_bits(W.bf16_bits_to_f32(w["kv_src"]) * np.float32(2.0 * scale))
