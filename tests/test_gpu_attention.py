@@ -296,6 +296,34 @@ def test_multi_sequence_page_tables():
     assert_attn_close(O, L, Or, Lr, "multi-seq")
 
 
+@pytest.mark.parametrize("page_size", [1, 16, 128, 256])
+@pytest.mark.parametrize("mode", ["raw512", "scaled528", "q8"])
+def test_page_sizes(page_size, mode):
+    """Index translation row = page_table[seq][i / P] * P + i % P at page sizes
+    other than the workloads' 64 (one row a page up to 256), over a shuffled
+    page table; decode over both layouts and the FP8-query prefill."""
+    rng = np.random.default_rng(400 + page_size)
+    pool_rows = 4096
+    w = _small(layout="scaled528" if mode == "scaled528" else "raw512", T=5, K=384, pool_rows=pool_rows,
+               seed=401 + page_size)
+    pages = pool_rows // page_size
+    w["page_table"] = rng.permutation(pages).astype(np.int32).reshape(1, pages)
+    w["page_size"] = page_size
+    w["topk"] = np.stack([rng.choice(pool_rows, 384, replace=False) for _ in range(5)]).astype(np.int32)
+    w["topk"][:, 300:] = -1
+    pool, pd = pool_for(w, ("page_size", page_size, mode))
+    if mode == "q8":
+        q8, qs = oracle.quantize_q8(w["q_bf16"])
+        O, L, err = run_prefill(w, pd, q8, qs)
+        Or, Lr, erro = oracle.sparse_attn(pool, "raw512", w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                                          page_table=w["page_table"], page_size=page_size)
+    else:
+        O, L, err = run_decode(w, pd)
+        Or, Lr, erro = oracle_decode(w, pool)
+    assert err == erro == 0
+    assert_attn_close(O, L, Or, Lr, f"page size {page_size} {mode}")
+
+
 def test_duplicates_and_scattered_sentinels():
     w = _small("scaled528", T=6, K=384, pool_rows=2048, masked_frac=0.3)
     w["topk"][:, 10:50] = w["topk"][:, 50:90]                    # many duplicates
