@@ -268,6 +268,33 @@ def test_topk_widths(K):
     assert_attn_close(O, L, Or, Lr, f"K={K}")
 
 
+@pytest.mark.parametrize("mode", ["raw512", "scaled528", "q8", "rope656"])
+def test_one_tile_segments(mode):
+    """Many tokens with one-tile lists (K = 128): every tile is a segment of its
+    own, so each CTA switches query buffers, resets the running state and runs
+    the epilogue on every tile, and the tail CTAs' units split across CTAs."""
+    T, H, K = 1000, 16, 128
+    rng = np.random.default_rng(500)
+    if mode == "rope656":
+        w = W.decode_rope656(seed=501, T=T, H=H, K=K, pool_rows=8192)
+    else:
+        w = _small(layout="scaled528" if mode == "scaled528" else "raw512", T=T, H=H, K=K, pool_rows=8192,
+                   seed=502)
+    w["topk"] = np.stack([rng.choice(8192, K, replace=False) for _ in range(T)]).astype(np.int32)
+    w["topk"][rng.random((T, K)) < 0.1] = -1
+    pool, pd = pool_for(w, ("one-tile", mode))
+    if mode == "q8":
+        q8, qs = oracle.quantize_q8(w["q_bf16"])
+        O, L, err = run_prefill(w, pd, q8, qs)
+        Or, Lr, erro = oracle.sparse_attn(pool, "raw512", w["topk"], w["sm_scale"], q8=q8, q_scale=qs,
+                                          page_table=w["page_table"], page_size=w["page_size"])
+    else:
+        O, L, err = run_decode(w, pd)
+        Or, Lr, erro = oracle_decode(w, pool)
+    assert err == erro == 0
+    assert_attn_close(O, L, Or, Lr, f"one-tile segments {mode}")
+
+
 @pytest.mark.parametrize("T,K,layout", [(1, 8192, "raw512"), (2, 16384, "raw512"), (1, 4096, "scaled528")])
 def test_unit_spread_over_many_ctas(T, K, layout):
     """Few tokens with long top-k lists: each (token, head group) is split over
