@@ -77,6 +77,23 @@ def test_gather_small_paged(layout, T, K):
     assert full == (T * K >= pool_rows)
 
 
+@pytest.mark.parametrize("page_size", [1, 16, 256])
+@pytest.mark.parametrize("T,K", [(4, 128), (20, 128)])
+def test_gather_page_sizes(page_size, T, K):
+    """Index translation at page sizes other than 64 over two sequences, in the
+    selected branch (4 x 128 entries over 2048 rows) and the full-pool branch
+    (20 x 128)."""
+    pool_rows = 2048
+    pool, rng = _pool("scaled528", pool_rows, 16 + page_size)
+    pages = pool_rows // page_size
+    page_table = rng.permutation(pages).astype(np.int32).reshape(2, -1)
+    token_seq = (np.arange(T) % 2).astype(np.int32)
+    topk = rng.integers(0, page_table.shape[1] * page_size, (T, K)).astype(np.int32)
+    topk[rng.random((T, K)) < 0.15] = -1
+    full = check(pool, "scaled528", topk, page_table=page_table, page_size=page_size, token_seq=token_seq)
+    assert full == (T * K >= pool_rows)
+
+
 @pytest.mark.parametrize("delta", [-1, 0, 1])
 def test_gather_branch_boundary(delta):
     """T*K = pool_rows - 1, pool_rows, pool_rows + 1 (physical indices): the
